@@ -152,6 +152,28 @@ static void softmax_pv_row(const double *s, double *p, int64_t n, const double *
     *lse = m + log(l);
 }
 
+/* The same three steps with the value rows already in fp64 (v: n rows of d). */
+static void softmax_pv_row_d(const double *s, double *p, int64_t n, const double *v, int d,
+                             double *o, double *lse) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) m = fmax(m, s[j]);
+    if (m == -INFINITY) {
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
+    for (int64_t j = 0; j < n; ++j) p[j] = exp(s[j] - m) / l;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        if (p[j] == 0.0) continue;
+        const double *vr = v + j * d;
+        for (int c = 0; c < d; ++c) o[c] += p[j] * vr[c];
+    }
+    *lse = m + log(l);
+}
+
 /*
  * Prefill attention for selected rows.  Layouts (contiguous, as on the CUDA side):
  *   q [B, Hq, Nq, d], k/v [B, Hkv, Nkv, d], storage bits of fp16 (dtype 0) or bf16 (1).
@@ -170,6 +192,19 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
     const int group = Hq / Hkv;
     const int64_t off = (int64_t)Nkv - (int64_t)Nq;
     int bad = 0;
+    /* Exact fp64 copies of K and V when they fit in 4 GiB (the values are the same either way;
+     * the copy only avoids converting each element once per query row). */
+    const int64_t kv_elems = (int64_t)B * Hkv * Nkv * d;
+    double *kd = NULL, *vd = NULL;
+    if (kv_elems > 0 && kv_elems * 16 <= ((int64_t)4 << 30)) {
+        kd = (double *)malloc(sizeof(double) * (size_t)kv_elems);
+        vd = (double *)malloc(sizeof(double) * (size_t)kv_elems);
+        if (kd && vd) {
+            for (int64_t x = 0; x < kv_elems; ++x) { kd[x] = tab[k[x]]; vd[x] = tab[v[x]]; }
+        } else {
+            free(kd); free(vd); kd = vd = NULL;
+        }
+    }
 #ifdef _OPENMP
     if (n_threads <= 0) n_threads = omp_get_max_threads();
 #pragma omp parallel num_threads(n_threads) reduction(| : bad)
@@ -196,20 +231,30 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
             const uint16_t *kp = k + (b * Hkv + hk) * (int64_t)Nkv * d;
             const uint16_t *vp = v + (b * Hkv + hk) * (int64_t)Nkv * d;
             for (int c = 0; c < d; ++c) qd[c] = tab[qp[c]];
+            const int64_t plane = (b * Hkv + hk) * (int64_t)Nkv * d;
             /* step 1: the row of S (masked entries are -inf) */
             for (int64_t j = 0; j < Nkv; ++j) {
                 vr[j] = vp + j * d;
                 if (causal && j > i + off) { s[j] = -INFINITY; continue; }
-                const uint16_t *kr = kp + j * d;
                 double acc = 0.0;
-                for (int c = 0; c < d; ++c) acc += qd[c] * tab[kr[c]];
+                if (kd) {
+                    const double *kr = kd + plane + j * d;
+                    for (int c = 0; c < d; ++c) acc += qd[c] * kr[c];
+                } else {
+                    const uint16_t *kr = kp + j * d;
+                    for (int c = 0; c < d; ++c) acc += qd[c] * tab[kr[c]];
+                }
                 s[j] = scale * acc;
             }
             /* steps 2 and 3: the row of P, then the row of O */
-            softmax_pv_row(s, p, Nkv, tab, vr, d, o + r * d, lse + r);
+            if (vd)
+                softmax_pv_row_d(s, p, Nkv, vd + plane, d, o + r * d, lse + r);
+            else
+                softmax_pv_row(s, p, Nkv, tab, vr, d, o + r * d, lse + r);
         }
         free(s); free(p); free(vr); free(qd);
     }
+    free(kd); free(vd);
     free(tab);
     return bad ? -1 : 0;
 }
