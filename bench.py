@@ -1,0 +1,515 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one prefill pass and one split-KV decode pass, each through the C ABI, on synthetic
+inputs of the pages' shapes already resident in device memory:
+  prefill: grouped-query causal prefill, B=1, Hq=64, Hkv=8, N=8192, d=128, bf16
+           (the 70B-class head shape), FLOPs counted as 4*B*Hq*N^2*d/2 (causal);
+  decode:  B=64 sequences, Hq=64, Hkv=8, d=128, bf16, lengths ~ U[1024, 32768] (seed 5000),
+           512-token splits, algorithmic bytes = K + V + q + o + lse.
+The headline ``value`` is prefill TFLOP/s (whole job: all ranks' FLOPs / the slowest rank's
+prefill time); decode GB/s is reported beside it under ``decode``.  Kernel durations come from
+CUDA events on the launching stream.  Both workloads are larger than L2 (302 MB and 4.4 GB), so
+no L2 flush is inserted between steps.
+
+``--impl reference`` times the fp64 CPU oracle (the reference definition) on a bounded sample of
+the same prefill workload, on this machine's host cores.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU (replicas, weak scaling);
+there is no collective on the data path.  A barrier and a max-over-ranks reduction frame the
+timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; decode KV-read GB/s & % HBM peak"
+
+
+# ----------------------------------------------------------------------------------------
+# distributed helpers (also used by the CPU gloo test)
+# ----------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(values, device=None):
+    """Element-wise max over ranks of a list of floats (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, world: int, device=None) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    (t_max,) = reduce_max([seconds_per_rank], device)
+    return units_per_rank * world / t_max
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[int(str(device).split(":")[1])])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------------------
+# peaks, clocks, profiles
+# ----------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(2 * self.period / 1000.0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sel = [l for t, l in self.lines if self.t_start is None or
+               (self.t_start - 0.06 <= t <= (self.t_stop or t) + 0.06)]
+        if not sel:
+            sel = [l for _, l in self.lines]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in sel:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {
+            "sm_mhz": float(np.median(sm)) if sm else None,
+            "sm_max_mhz": float(max(smax)) if smax else None,
+            "power_w_max": float(max(power)) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_sha") != source_sha(sources):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+FWD_SOURCES = ["exact_io_aware_09_gb300/csrc/attn_fwd.cu", "exact_io_aware_09_gb300/csrc/ptx.cuh",
+               "exact_io_aware_09_gb300/csrc/internal.h"]
+DEC_SOURCES = ["exact_io_aware_09_gb300/csrc/attn_decode.cu", "exact_io_aware_09_gb300/csrc/ptx.cuh",
+               "exact_io_aware_09_gb300/csrc/internal.h"]
+
+
+# ----------------------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ----------------------------------------------------------------------------------------
+def prefill_sample_rows(cfg, n_rows, seed=0):
+    rng = np.random.default_rng(seed)
+    n = cfg.B * cfg.Hq * cfg.N_q
+    return np.sort(rng.choice(n, size=n_rows, replace=False)).astype(np.int64)
+
+
+def row_flops(cfg, rows):
+    """Exact FLOPs of the selected rows: 4*d per visible key (2 for Q K^T, 2 for P V)."""
+    i = rows % cfg.N_q
+    vis = np.minimum(i + (cfg.N_kv - cfg.N_q) + 1, cfg.N_kv) if cfg.causal else np.full_like(i, cfg.N_kv)
+    return float(4.0 * cfg.d * np.clip(vis, 0, None).sum())
+
+
+def time_oracle_prefill(cfg, q, k, v, budget_s=12.0, rows_per_batch=64, seed=0):
+    import oracle
+
+    rng_seed = seed
+    done_flops, t_total, n_rows = 0.0, 0.0, 0
+    while t_total < budget_s:
+        rows = prefill_sample_rows(cfg, rows_per_batch, rng_seed)
+        rng_seed += 1
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q, cfg.N_kv,
+                              cfg.d, cfg.causal, cfg.scale, rows)
+        t_total += time.perf_counter() - t0
+        done_flops += row_flops(cfg, rows)
+        n_rows += len(rows)
+    return done_flops / t_total / 1e12, n_rows, t_total
+
+
+# ----------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import exact_io_aware_09_gb300 as attn
+    import synthetic as syn
+
+    rank, world, local = dist_env()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    peaks, peak_src = load_peaks()
+
+    pcfg = syn.CONFIG4
+    dcfg = syn.CONFIG5
+    q, k, v = pcfg.device_inputs(device)
+    o = torch.empty_like(q)
+    lse = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), device=device, dtype=torch.float32)
+    lengths = dcfg.lengths()
+    cu = torch.from_numpy(syn.cu_seqlens(lengths)).to(device)
+    max_len = int(lengths.max())
+    dq, dk, dv = dcfg.device_inputs(device)
+    do = torch.empty_like(dq)
+    dl = torch.empty((dcfg.B, dcfg.Hq), device=device, dtype=torch.float32)
+    ws = torch.empty(attn.attn_decode_workspace_bytes(dcfg.B, dcfg.Hq, max_len, dcfg.split, dcfg.d),
+                     device=device, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        attn.attn_fwd(q, k, v, o=o, lse=lse, causal=True, scale=pcfg.scale, stream=stream)
+
+    def decode():
+        attn.attn_decode_splitkv(dq, dk, dv, cu, max_len, o=do, lse=dl, split_size=dcfg.split,
+                                 scale=dcfg.scale, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    st = attn.attn_poll_status()
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {attn.attn_status_string(st)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    barrier(device)
+    torch.cuda.synchronize()
+    sampler.mark("start")
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        prefill()
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    barrier(device)
+    sampler.mark("stop")
+    clocks = sampler.stop()
+    st = attn.attn_poll_status()
+    if st != 0:
+        raise SystemExit(f"device status after timing: {attn.attn_status_string(st)}")
+    pre_ms = float(sum(e[0].elapsed_time(e[1]) for e in ev))
+    dec_ms = float(sum(e[1].elapsed_time(e[2]) for e in ev))
+    step_ms = float(ev[0][0].elapsed_time(ev[-1][2]))
+    pre_ms_max, dec_ms_max, step_ms_max, wall_max = reduce_max([pre_ms, dec_ms, step_ms, t_wall], device)
+
+    flops = pcfg.flops()
+    kv_bytes = dcfg.kv_bytes()
+    dec_bytes = kv_bytes + 2 * dq.numel() * 2 + dl.numel() * 4
+    value = flops * args.steps * world / (pre_ms_max / 1e3) / 1e12
+    dec_gbs = dec_bytes * args.steps * world / (dec_ms_max / 1e3) / 1e9
+    # per-launch rooflines of this rank's kernels
+    pre_launch_s = pre_ms / args.steps / 1e3
+    dec_launch_s = dec_ms / args.steps / 1e3
+    ach_t = flops / pre_launch_s / 1e12
+    ach_b = dec_bytes / dec_launch_s / 1e9
+
+    # end to end through the public API with host buffers: H2D inputs, call, D2H result
+    e2e = run_e2e(args, attn, pcfg, q, k, v, stream, device, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(pcfg, q, k, v)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), drawn on device)",
+        "config": {
+            "workload": "gqa causal prefill B=1 Hq=64 Hkv=8 N=8192 d=128 bf16 + split-KV decode "
+                        "B=64 Hq=64 Hkv=8 d=128 bf16 L~U[1024,32768] split=512",
+            "prefill": pcfg.name, "decode": dcfg.name,
+            "prefill_flops_per_step": flops, "decode_bytes_per_step": dec_bytes,
+            "l2": "no flush: inputs larger than L2 (prefill 302 MB, decode 4.43 GB per step)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "kernel": "attn_fwd_kernel<128,bf16>",
+            "bound": "tensor",
+            "achieved": round(ach_t, 2),
+            "peak": peaks["bf16_tflops"],
+            "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+            "unit": "TFLOP/s",
+            "frac": round(ach_t / peaks["bf16_tflops"], 4),
+            "frac_of_spec_2250": round(ach_t / 2250.0, 4),
+            "traffic": profiled_traffic("attn_fwd_kernel", FWD_SOURCES),
+            # compulsory bytes of one launch: Q, K, V read, O written (2 B each), LSE (4 B)
+            "algorithmic_bytes": int((2 * q.numel() + 2 * k.numel()) * 2 + lse.numel() * 4),
+        },
+        "decode": {
+            "value": round(dec_gbs, 1),
+            "unit": "GB/s",
+            "ms_per_launch": round(dec_ms / args.steps, 4),
+            "roofline": {
+                "kernel": "attn_decode_split_kernel + attn_decode_merge_kernel",
+                "bound": "hbm",
+                "achieved": round(ach_b, 1),
+                "peak": peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} HBM copy",
+                "unit": "GB/s",
+                "frac": round(ach_b / peaks["hbm_gbs"], 4),
+                "frac_of_spec_8000": round(ach_b / 8000.0, 4),
+                "traffic": profiled_traffic("attn_decode_split_kernel", DEC_SOURCES),
+            },
+        },
+        "prefill_ms_per_launch": round(pre_ms / args.steps, 4),
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall_max, 4),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, attn, pcfg, q, k, v, stream, device, world):
+    import torch
+
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+    hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    hq.copy_(q)
+    hk.copy_(k)
+    hv.copy_(v)
+    ho = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hl = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), dtype=torch.float32, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    do = torch.empty_like(q)
+    dl = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), device=device, dtype=torch.float32)
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        attn.attn_fwd(dq, dk, dv, o=do, lse=dl, causal=True, scale=pcfg.scale, stream=stream)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    (ms_max,) = reduce_max([ms], device)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = q.numel() * 2 + dl.numel() * 4
+    return {
+        "value": round(pcfg.flops() * steps * world / (ms_max / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "h2d_bytes_per_step": int(h2d),
+        "d2h_bytes_per_step": int(d2h),
+        "steps": steps,
+        "ms_per_step": round(ms_max / steps, 4),
+    }
+
+
+def cpu_baseline_prefill(pcfg, q, k, v, budget_s=12.0):
+    import oracle
+    import synthetic as syn
+
+    qb, kb, vb = (syn.tensor_to_bits(t) for t in (q, k, v))
+    tflops, n_rows, t = time_oracle_prefill(pcfg, qb, kb, vb, budget_s)
+    return {
+        "value": round(tflops, 6),
+        "unit": "TFLOP/s",
+        "cores": oracle.max_threads(),
+        "kind": "oracle",
+        "sample": f"{n_rows} random query rows of the prefill workload ({t:.1f} s, exact per-row "
+                  f"FLOPs 4*d*visible keys), fp64",
+    }
+
+
+# ----------------------------------------------------------------------------------------
+# reference arm: the oracle as it stands, on the host cores
+# ----------------------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synthetic as syn
+
+    pcfg = syn.CONFIG4
+    q, k, v = pcfg.host_inputs()
+    rows_per_step = 16
+    for i in range(args.warmup):
+        oracle.attention_rows(q, k, v, pcfg.dtype, pcfg.B, pcfg.Hq, pcfg.Hkv, pcfg.N_q, pcfg.N_kv,
+                              pcfg.d, True, pcfg.scale, prefill_sample_rows(pcfg, rows_per_step, 10_000 + i))
+    flops, t = 0.0, 0.0
+    for i in range(args.steps):
+        rows = prefill_sample_rows(pcfg, rows_per_step, i)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, pcfg.dtype, pcfg.B, pcfg.Hq, pcfg.Hkv, pcfg.N_q, pcfg.N_kv,
+                              pcfg.d, True, pcfg.scale, rows)
+        t += time.perf_counter() - t0
+        flops += row_flops(pcfg, rows)
+    value = flops / t / 1e12
+    sample = (f"{rows_per_step} random query rows of the prefill workload per step "
+              f"(exact per-row FLOPs), fp64 oracle")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), drawn on host)",
+        "config": {"workload": "gqa causal prefill B=1 Hq=64 Hkv=8 N=8192 d=128 bf16 (sampled rows)",
+                   "prefill": pcfg.name},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+"""Python binding of libattn_gb300.so (exact attention for GB300 / sm_103a).
+
+The functions below only marshal arguments (torch tensors -> device pointers, sizes, the
+current CUDA stream) and call the C ABI declared in ``include/attn.h``; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU or PyTorch fallback: if the
+library is missing the import fails, and an unsupported request raises ``AttnError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes",
+    "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_selftest_timeout",
+    "attn_version", "library_path", "lib",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libattn_gb300.so")
+
+if not os.path.exists(library_path):
+    raise ImportError(
+        f"{library_path} is missing: build it first (python exact_io_aware_09_gb300/build.py "
+        "or __graft_entry__.build()); there is no fallback implementation")
+
+lib = ctypes.CDLL(library_path)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
+lib.attn_fwd.restype = _I
+lib.attn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+lib.attn_decode_workspace_bytes.restype = _SZ
+lib.attn_decode_splitkv.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _F, _I,
+                                    _P, _SZ, _P]
+lib.attn_decode_splitkv.restype = _I
+lib.attn_poll_status.argtypes = [_P]
+lib.attn_poll_status.restype = _I
+lib.attn_status_string.argtypes = [_I]
+lib.attn_status_string.restype = ctypes.c_char_p
+lib.attn_fwd_kv_tiles.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+lib.attn_fwd_kv_tiles.restype = _I
+lib.attn_selftest_timeout.argtypes = [_I, _P]
+lib.attn_selftest_timeout.restype = _I
+lib.attn_version.argtypes = []
+lib.attn_version.restype = ctypes.c_char_p
+
+ATTN_F16, ATTN_BF16 = 0, 1
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def attn_status_string(status: int) -> str:
+    return lib.attn_status_string(int(status)).decode()
+
+
+def attn_version() -> str:
+    return lib.attn_version().decode()
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise AttnError(-2, f"dtype {t.dtype}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _dev_ptr(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise AttnError(-1, f"{name} must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+             stream=None):
+    """Exact attention forward.  q [B,Hq,N_q,d], k/v [B,Hkv,N_kv,d] fp16/bf16 CUDA tensors.
+
+    Returns (o [B,Hq,N_q,d] same dtype, lse [B,Hq,N_q] fp32).  Enqueued on ``stream``
+    (default: torch's current stream); no synchronisation.
+    """
+    torch = _torch()
+    B, Hq, N_q, d = q.shape
+    _, Hkv, N_kv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise AttnError(-1, "attn_fwd: q/k/v shapes or dtypes disagree")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N_q), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib.attn_fwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                      _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(bool(causal)),
+                      float(scale), _stream_handle(stream), _dtype_code(q))
+    _check(st, "attn_fwd")
+    return o, lse
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, max_seqlen_k: int, split_size: int, d: int) -> int:
+    return int(lib.attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d))
+
+
+def attn_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, max_seqlen_k: int, o=None, lse=None,
+                        split_size: int = 512, scale: float | None = None, workspace=None,
+                        stream=None):
+    """One split-KV decode step.
+
+    q [B,Hq,d]; k_cache/v_cache [capacity,Hkv,d]; cu_seqlens_k int32 CUDA [B+1].
+    ``workspace``: a uint8 CUDA tensor of at least attn_decode_workspace_bytes(...) bytes
+    (allocated here when omitted).  Returns (o [B,Hq,d], lse [B,Hq] fp32).
+    """
+    torch = _torch()
+    B, Hq, d = q.shape
+    cap, Hkv, _ = k_cache.shape
+    if cu_seqlens_k.dtype != torch.int32 or cu_seqlens_k.numel() != B + 1:
+        raise AttnError(-1, "attn_decode_splitkv: cu_seqlens_k must be int32 [B+1]")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    st = lib.attn_decode_splitkv(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+                                 _dev_ptr(v_cache, "v_cache"), _dev_ptr(cu_seqlens_k, "cu_seqlens_k"),
+                                 cap, int(max_seqlen_k), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B,
+                                 Hq, Hkv, d, int(split_size), float(scale), _dtype_code(q),
+                                 _dev_ptr(workspace, "workspace"), workspace.numel(),
+                                 _stream_handle(stream))
+    _check(st, "attn_decode_splitkv")
+    return o, lse
+
+
+def attn_poll_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(lib.attn_poll_status(_stream_handle(stream)))
+
+
+def attn_fwd_kv_tiles(q_tile: int, block_m: int, block_n: int, N_q: int, N_kv: int, causal: bool):
+    """(n_tiles, first_masked) of the prefill schedule for one query tile (host only)."""
+    n = _I(0)
+    fm = _I(0)
+    _check(lib.attn_fwd_kv_tiles(q_tile, block_m, block_n, N_q, N_kv, int(bool(causal)),
+                                 ctypes.byref(n), ctypes.byref(fm)), "attn_fwd_kv_tiles")
+    return n.value, fm.value
+
+
+def attn_selftest_timeout(limit_us: int, stream=None) -> None:
+    _check(lib.attn_selftest_timeout(int(limit_us), _stream_handle(stream)), "attn_selftest_timeout")

@@ -1,0 +1,210 @@
+// C ABI of libattn_gb300.so: argument checks, TMA descriptors, the device status word and the
+// timeout self-test.  The kernels live in attn_fwd.cu and attn_decode.cu.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+__device__ int g_status;  // first device-side error since the last attn_poll_status
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The kernels use tcgen05 and are built for sm_103a only.
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  static int checked[kMaxDevices];  // 0 unknown, 1 ok, 2 not usable
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  if (checked[dev] == 0) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+    checked[dev] = (prop.major == 10 && prop.minor == 3) ? 1 : 2;
+  }
+  return checked[dev] == 1 ? ATTN_OK : ATTN_ERR_DEVICE;
+}
+
+}  // namespace
+
+bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, uint64_t dim1,
+                  uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                  uint32_t box1, uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || dim0 == 0 || dim1 == 0 || dim2 == 0) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+// Waits on a barrier no one arrives at, for `limit_ns`, then latches the time-out status.
+__global__ void selftest_timeout_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  wait_bounded(smem_u32(&bar), 0, nullptr, status, limit_ns);
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N_q, int N_kv, int d, int causal, float scale, attn_stream_t stream,
+             attn_dtype_t dtype) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N_q < 0 || N_kv < 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || N_q == 0) return ATTN_OK;
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse) ||
+      (N_kv > 0 && (!aligned16(k) || !aligned16(v))))
+    return ATTN_ERR_MISALIGNED;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale, dtype == ATTN_BF16};
+  return launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_size, int d) {
+  return decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
+}
+
+int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* cu_seqlens_k, int kv_capacity, int max_seqlen_k, void* o,
+                        float* lse, int B, int Hq, int Hkv, int d, int split_size, float scale,
+                        attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                        attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || kv_capacity < 0 || max_seqlen_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!q || !o || !lse || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+  if (max_seqlen_k > 0 && kv_capacity > 0 && (!k_cache || !v_cache)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  DecodeArgs a{q, k_cache, v_cache, cu_seqlens_k, kv_capacity, max_seqlen_k, o, lse, B,
+               Hq, Hkv, d, split_size, scale, dtype == ATTN_BF16, workspace};
+  return launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_poll_status(attn_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  int* dp = device_status_ptr();
+  if (!dp) return ATTN_ERR_LAUNCH;
+  int st = 0;
+  if (cudaMemcpy(&st, dp, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if (st != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dp, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
+  return st;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_LAUNCH: return "kernel launch or tensor map failed";
+    case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    case ATTN_ERR_DEVICE: return "no usable sm_103 device";
+    case ATTN_ERR_BAD_LENGTHS: return "a sequence length exceeds max_seqlen_k or kv_capacity";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd_kv_tiles(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
+                      int* n_tiles, int* first_masked) {
+  if (q_tile < 0 || block_m <= 0 || block_n <= 0 || N_q < 0 || N_kv < 0 || !n_tiles ||
+      !first_masked)
+    return ATTN_ERR_INVALID_ARG;
+  int n = 0, fm = 0;
+  kv_tile_range(q_tile, block_m, block_n, N_q, N_kv, causal ? 1 : 0, n, fm);
+  *n_tiles = n;
+  *first_masked = fm;
+  return ATTN_OK;
+}
+
+int attn_selftest_timeout(int limit_us, attn_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  int* st = device_status_ptr();
+  if (!st) return ATTN_ERR_LAUNCH;
+  selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      st, static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+const char* attn_version(void) { return "attn_gb300 0.1 (sm_103a; tcgen05 prefill, split-KV decode)"; }
+
+}  // extern "C"

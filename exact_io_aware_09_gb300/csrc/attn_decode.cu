@@ -1,0 +1,401 @@
+// Split-KV decode: one new query token per sequence attends to its whole packed KV cache.
+//
+// "FlashAttention Explained", section "Decoding, Paged and Split-KV Variants", and "FlashAttention
+// and GPU Data Movement", section 6.1: with one query row the query axis gives no parallelism, so
+// the key/value sequence is split into chunks processed by separate thread blocks; each chunk
+// yields a partial state (m, l, o) and the partial states are merged exactly with the block-merge
+// rule of "How FlashAttention Reduces HBM Traffic Exactly", section "Why softmax does not prevent
+// tiling".
+//
+// Kernel 1 (split): block (split s, key/value head hk, sequence b).  A producer warp streams the
+// chunk's K and V rows of head hk through a ring of 64-token stages with TMA (the cache is
+// [tokens, Hkv, d], so one stage is 64 strided 2*d-byte rows per tensor).  Four compute warps
+// each take 16 tokens of every stage and run the online softmax for the G = Hq/Hkv query heads
+// that share hk.  The per-token work is tiny (8 FLOP per cache byte) and the kernel is bound by
+// HBM, so the two small products run on warp-level mma.sync tiles (m16n8k16, query heads padded
+// to 16 rows) straight from the swizzled stage buffers.  The four warps' states are merged in
+// shared memory and the chunk's normalised (m, l, o) is written to the workspace.
+// Kernel 2 (merge): one block per (sequence, query head) merges that row's chunk states.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kDecTok = 64;      // tokens per ring stage
+constexpr int kDecWarps = 4;     // compute warps, 16 tokens of each stage apiece
+constexpr int kDecThreads = 160;  // + one producer warp
+constexpr int kDecStages = 3;
+constexpr int kMaxGroup = 16;    // query heads per key/value head (rows of the m16 tile)
+
+struct DecParams {
+  const uint16_t* q;   // [B, Hq, D]
+  const int32_t* cu;   // [B + 1]
+  float* ws_o;         // [B * Hq * max_splits, D]  normalised partial outputs
+  float* ws_ml;        // [B * Hq * max_splits, 2]  (m in log2 units, l)
+  int* status;
+  int Hq, Hkv, G, capacity, max_seqlen, split, max_splits;
+  float sl2;
+};
+
+template <int D>
+struct DecLayout {
+  static constexpr uint32_t kHalf = kDecTok * 128;             // one 64-column half of a stage
+  static constexpr uint32_t kTensor = (D / 64) * kHalf;         // K or V of one stage
+  static constexpr uint32_t kStage = 2 * kTensor;
+  static constexpr uint32_t kRing = kDecStages * kStage;
+  static constexpr uint32_t kRed = kDecWarps * kMaxGroup * (D + 2) * 4;  // reuses the ring
+  static_assert(kRed <= kRing, "merge scratch must fit in the ring");
+  static constexpr uint32_t kBar = kRing;                        // full[S], empty[S]
+  static constexpr uint32_t kMisc = kBar + 2 * kDecStages * 8;   // abort flag
+  static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+};
+
+__device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              int* status) {
+  const bool ok = wait_bounded(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool lengths_ok(const DecParams& p, int t_start, int t_stop) {
+  const int len = t_stop - t_start;
+  return t_start >= 0 && len >= 0 && len <= p.max_seqlen && t_stop <= p.capacity;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDecThreads)
+    attn_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
+  using L = DecLayout<D>;
+  const int split = blockIdx.x;
+  const int hk = blockIdx.y;
+  const int b = blockIdx.z;
+  const int t_start = p.cu[b];
+  const int t_stop = p.cu[b + 1];
+  if (!lengths_ok(p, t_start, t_stop)) {
+    if (split == 0 && hk == 0 && threadIdx.x == 0) latch_status(p.status, kStatusBadLengths);
+    return;
+  }
+  const int len = t_stop - t_start;
+  const int n_splits = (len + p.split - 1) / p.split;
+  if (split >= n_splits) return;
+  const int t0 = t_start + split * p.split;
+  const int n_tok = min(p.split, t_stop - t0);
+  const int n_stages = (n_tok + kDecTok - 1) / kDecTok;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + L::kBar;
+#define FULL(s) (bars + 8u * (s))
+#define EMPTY(s) (bars + 8u * (kDecStages + (s)))
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), kDecWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int st = 0; st < n_stages; ++st) {
+        const int s = st % kDecStages;
+        if (st >= kDecStages &&
+            !wait_bounded(EMPTY(s), ((st / kDecStages) - 1) & 1, abort_flag, p.status))
+          break;
+        const uint32_t kbuf = base + s * L::kStage;
+        const uint32_t vbuf = kbuf + L::kTensor;
+        mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) {
+          tma_load_3d(kbuf + hh * L::kHalf, &tm_k, FULL(s), hh * 64, hk, t0 + st * kDecTok);
+          tma_load_3d(vbuf + hh * L::kHalf, &tm_v, FULL(s), hh * 64, hk, t0 + st * kDecTok);
+        }
+        issued = st + 1;
+      }
+      for (int st = (issued > kDecStages ? issued - kDecStages : 0); st < issued; ++st)
+        wait_bounded(FULL(st % kDecStages), (st / kDecStages) & 1, nullptr, p.status,
+                     100000000ull);
+    }
+    return;  // the producer takes no part in the reduction below
+  }
+
+  // -------------------------------------------------------------------- compute warps
+  const int g = lane >> 2;  // accumulator row (query head inside the group) and +8
+  const int c = lane & 3;
+  const int hq0 = hk * p.G;
+  const bool row0 = g < p.G, row1 = g + 8 < p.G;
+  const uint16_t* qb = p.q + (static_cast<size_t>(b) * p.Hq + hq0) * D;
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int col = ks * 16 + 2 * c;
+    qa[ks][0] = row0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + col) : 0u;
+    qa[ks][1] = row1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + col) : 0u;
+    qa[ks][2] = row0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + col + 8) : 0u;
+    qa[ks][3] = row1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + col + 8) : 0u;
+  }
+  float m[2] = {-INFINITY, -INFINITY};
+  float l[2] = {0.f, 0.f};  // partial over this thread's columns
+  float o[D / 8][4];
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+
+  bool ok = true;
+  for (int st = 0; st < n_stages; ++st) {
+    const int s = st % kDecStages;
+    if (!dec_warp_wait(FULL(s), (st / kDecStages) & 1, abort_flag, p.status)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kbuf = base + s * L::kStage;
+    const uint32_t vbuf = kbuf + L::kTensor;
+    const int key0 = st * kDecTok + warp * 16;  // first token of this warp, chunk-relative
+    const int valid = n_tok - key0;             // tokens of this warp that belong to the chunk
+    if (valid > 0) {
+      if (valid < 16) {
+        // Rows past the chunk hold other sequences' (or unwritten) cache rows: zero their V so
+        // 0 * V stays 0 even for non-finite garbage.
+        for (int i = lane; i < (16 - valid) * (D / 8); i += 32) {
+          const int rr = warp * 16 + valid + i / (D / 8);
+          const int ch = i % (D / 8);
+          *reinterpret_cast<uint4*>(gbase + (vbuf - base) + (ch >> 3) * L::kHalf + sw128(rr, ch & 7)) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // S = Q K^T for this warp's 16 tokens: two n8 tiles.
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int chunk = ks * 2 + ((lane >> 3) & 1);
+        const int key = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
+        uint32_t b00, b01, b10, b11;
+        ldmatrix_x4(kbuf + (chunk >> 3) * L::kHalf + sw128(key, chunk & 7), b00, b01, b10, b11);
+        mma_m16n8k16<BF16>(sc[0], qa[ks], b00, b01);
+        mma_m16n8k16<BF16>(sc[1], qa[ks], b10, b11);
+      }
+      // Online softmax for rows g and g + 8 over the 16 tokens ("FlashAttention and GPU Data
+      // Movement", section 3.1), base 2 with the scale folded in.
+      float x[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kidx = nt * 8 + 2 * c + (e & 1);
+          x[nt][e] = (kidx < valid) ? sc[nt][e] * p.sl2 : -INFINITY;
+        }
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float a0 = (m[0] == -INFINITY) ? 0.f : ex2(m[0] - mn0);
+      const float a1 = (m[1] == -INFINITY) ? 0.f : ex2(m[1] - mn1);
+      const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      m[0] = mn0;
+      m[1] = mn1;
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = ex2(x[nt][0] - mu0);
+        pr[nt][1] = ex2(x[nt][1] - mu0);
+        pr[nt][2] = ex2(x[nt][2] - mu1);
+        pr[nt][3] = ex2(x[nt][3] - mu1);
+      }
+      l[0] = l[0] * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+      l[1] = l[1] * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        o[nd][0] *= a0;
+        o[nd][1] *= a0;
+        o[nd][2] *= a1;
+        o[nd][3] *= a1;
+      }
+      // O += P V: P (16 rows x 16 tokens) comes straight from the score fragments.
+      uint32_t pa[4];
+      pa[0] = pack2<BF16>(pr[0][0], pr[0][1]);
+      pa[1] = pack2<BF16>(pr[0][2], pr[0][3]);
+      pa[2] = pack2<BF16>(pr[1][0], pr[1][1]);
+      pa[3] = pack2<BF16>(pr[1][2], pr[1][3]);
+#pragma unroll
+      for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+        const int key = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int chunk = nd2 * 2 + (lane >> 4);
+        uint32_t v0, v1, v2, v3;
+        ldmatrix_x4_trans(vbuf + (chunk >> 3) * L::kHalf + sw128(key, chunk & 7), v0, v1, v2, v3);
+        mma_m16n8k16<BF16>(o[2 * nd2], pa, v0, v1);
+        mma_m16n8k16<BF16>(o[2 * nd2 + 1], pa, v2, v3);
+      }
+      if (valid < 16) fence_proxy_async_smem();  // generic zeros before the next TMA write
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(EMPTY(s));
+  }
+
+  // ---------------------------------------------------- merge the four warps' states
+  l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+  l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+  l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+  l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+  named_bar_sync(1, kDecWarps * 32);  // every warp is done with the ring
+  ok = ok && (*abort_flag == 0);
+  float* red = reinterpret_cast<float*>(gbase);  // [warp][row][D + 2]
+  constexpr int kRow = D + 2;
+  if (ok) {
+    float* rw = red + warp * kMaxGroup * kRow;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      if (row0) {
+        rw[g * kRow + nd * 8 + 2 * c] = o[nd][0];
+        rw[g * kRow + nd * 8 + 2 * c + 1] = o[nd][1];
+      }
+      if (row1) {
+        rw[(g + 8) * kRow + nd * 8 + 2 * c] = o[nd][2];
+        rw[(g + 8) * kRow + nd * 8 + 2 * c + 1] = o[nd][3];
+      }
+    }
+    if (c == 0) {
+      if (row0) {
+        rw[g * kRow + D] = m[0];
+        rw[g * kRow + D + 1] = l[0];
+      }
+      if (row1) {
+        rw[(g + 8) * kRow + D] = m[1];
+        rw[(g + 8) * kRow + D + 1] = l[1];
+      }
+    }
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  if (ok) {
+    const size_t part0 = (static_cast<size_t>(b) * p.Hq + hq0) * p.max_splits + split;
+    for (int i = threadIdx.x; i < p.G * D; i += kDecWarps * 32) {
+      const int row = i / D, col = i % D;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, red[(w * kMaxGroup + row) * kRow + D]);
+      float ll = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = red[(w * kMaxGroup + row) * kRow + D];
+        const float wgt = (mw == -INFINITY) ? 0.f : ex2(mw - mm);
+        ll += wgt * red[(w * kMaxGroup + row) * kRow + D + 1];
+        acc += wgt * red[(w * kMaxGroup + row) * kRow + col];
+      }
+      const size_t part = part0 + static_cast<size_t>(row) * p.max_splits;
+      p.ws_o[part * D + col] = acc / ll;
+      if (col == 0) {
+        p.ws_ml[part * 2] = mm;
+        p.ws_ml[part * 2 + 1] = ll;
+      }
+    }
+  }
+#undef FULL
+#undef EMPTY
+}
+
+// Merge the chunk states of one (sequence, query head) row:
+//   m = max_s m_s,  w_s = 2^(m_s - m) l_s,  l = sum_s w_s,  o = sum_s w_s o_s / l,
+//   L = ln 2 * (m + log2 l).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(D)
+    attn_decode_merge_kernel(const DecParams p, uint16_t* out, float* lse) {
+  const int hq = blockIdx.x;
+  const int b = blockIdx.y;
+  const int col = threadIdx.x;
+  const int t_start = p.cu[b];
+  const int t_stop = p.cu[b + 1];
+  if (!lengths_ok(p, t_start, t_stop)) return;
+  const int n_splits = (t_stop - t_start + p.split - 1) / p.split;
+  const size_t row = static_cast<size_t>(b) * p.Hq + hq;
+  if (n_splits == 0) {
+    out[row * D + col] = 0;
+    if (col == 0) lse[row] = -INFINITY;
+    return;
+  }
+  const size_t part0 = row * p.max_splits;
+  float mm = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) mm = fmaxf(mm, p.ws_ml[(part0 + s) * 2]);
+  float ll = 0.f, acc = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float w = ex2(p.ws_ml[(part0 + s) * 2] - mm) * p.ws_ml[(part0 + s) * 2 + 1];
+    ll += w;
+    acc += w * p.ws_o[(part0 + s) * D + col];
+  }
+  const float v = acc / ll;
+  uint32_t pk = pack2<BF16>(v, 0.f);
+  out[row * D + col] = static_cast<uint16_t>(pk & 0xffffu);
+  if (col == 0) lse[row] = (mm + lg2(ll)) * 0.69314718055994531f;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int max_seqlen, int split, int d) {
+  if (B <= 0 || Hq <= 0 || max_seqlen < 0 || split <= 0 || d <= 0) return 0;
+  const size_t max_splits = (static_cast<size_t>(max_seqlen) + split - 1) / split;
+  const size_t parts = static_cast<size_t>(B) * Hq * (max_splits > 0 ? max_splits : 1);
+  const size_t o_bytes = (parts * d * 4 + 255) & ~static_cast<size_t>(255);
+  return o_bytes + parts * 2 * 4;
+}
+
+template <int D, bool BF16>
+static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
+  using L = DecLayout<D>;
+  const int max_splits = (a.max_seqlen + a.split - 1) / a.split;
+  const bool any_keys = a.kv_capacity > 0 && max_splits > 0;
+  CUtensorMap tk, tv;
+  const uint64_t row = static_cast<uint64_t>(D) * 2;
+  if (any_keys &&
+      (!make_tmap_3d(&tk, a.k_cache, BF16, D, a.Hkv, a.kv_capacity, row, row * a.Hkv, 64, 1, kDecTok) ||
+       !make_tmap_3d(&tv, a.v_cache, BF16, D, a.Hkv, a.kv_capacity, row, row * a.Hkv, 64, 1, kDecTok)))
+    return -5;
+  DecParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.cu = a.cu_seqlens;
+  const size_t parts = static_cast<size_t>(a.B) * a.Hq * (max_splits > 0 ? max_splits : 1);
+  p.ws_o = static_cast<float*>(a.workspace);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(a.workspace) +
+                                     ((parts * D * 4 + 255) & ~static_cast<size_t>(255)));
+  p.status = device_status_ptr();
+  if (!p.status) return -5;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.capacity = a.kv_capacity;
+  p.max_seqlen = a.max_seqlen;
+  p.split = a.split;
+  p.max_splits = max_splits > 0 ? max_splits : 1;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  auto kern = attn_decode_split_kernel<D, BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
+      cudaSuccess)
+    return -5;
+  if (any_keys) {
+    dim3 grid(max_splits, a.Hkv, a.B);
+    kern<<<grid, kDecThreads, L::kBytes, stream>>>(tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return -5;
+  }
+  dim3 mgrid(a.Hq, a.B);
+  attn_decode_merge_kernel<D, BF16><<<mgrid, D, 0, stream>>>(p, static_cast<uint16_t*>(a.o), a.lse);
+  return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.d == 64)
+    return a.bf16 ? launch_decode_variant<64, true>(a, stream) : launch_decode_variant<64, false>(a, stream);
+  if (a.d == 128)
+    return a.bf16 ? launch_decode_variant<128, true>(a, stream) : launch_decode_variant<128, false>(a, stream);
+  return -2;
+}
+
+}  // namespace attn

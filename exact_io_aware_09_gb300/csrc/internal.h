@@ -1,0 +1,81 @@
+// Host-side declarations shared by the translation units of libattn_gb300.so.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Encode a 3-D tiled TMA descriptor over a contiguous 16-bit tensor with dimensions
+// {dim0 (innermost, elements), dim1, dim2}, byte strides {stride1, stride2}, a box of
+// {box0, box1, box2} elements and the 128-byte swizzle.  Returns false on failure.
+bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, uint64_t dim1,
+                  uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                  uint32_t box1, uint32_t box2);
+
+// Device address of the status word of the current device (nullptr on failure).
+int* device_status_ptr();
+
+// Query tile range of the prefill schedule (also exported through the C ABI).
+__host__ __device__ inline void kv_tile_range(int qt, int bm, int bn, int n_q, int n_kv,
+                                              int causal, int& n_tiles, int& first_masked) {
+  const long long n_all = (static_cast<long long>(n_kv) + bn - 1) / bn;
+  const long long ragged_last = (n_kv % bn) ? n_all - 1 : n_all;
+  if (!causal) {
+    n_tiles = static_cast<int>(n_all);
+    first_masked = static_cast<int>(ragged_last);
+    return;
+  }
+  const long long off = static_cast<long long>(n_kv) - n_q;
+  const long long r_first = static_cast<long long>(qt) * bm;
+  long long r_last = static_cast<long long>(qt + 1) * bm;
+  if (r_last > n_q) r_last = n_q;
+  r_last -= 1;
+  const long long kmax = r_last + off;  // last key the last row of the tile may see
+  if (kmax < 0 || n_all == 0) {
+    n_tiles = 0;
+    first_masked = 0;
+    return;
+  }
+  long long n = kmax / bn + 1;
+  if (n > n_all) n = n_all;
+  const long long kmin = r_first + off;  // last key the first row of the tile may see
+  long long fm = (kmin + 1 >= 0) ? (kmin + 1) / bn : 0;  // tiles every row sees in full
+  if (fm > ragged_last) fm = ragged_last;
+  if (fm > n) fm = n;
+  n_tiles = static_cast<int>(n);
+  first_masked = static_cast<int>(fm);
+}
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, N_q, N_kv, d, causal;
+  float scale;
+  bool bf16;
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* cu_seqlens;
+  int kv_capacity, max_seqlen;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, d, split;
+  float scale;
+  bool bf16;
+  void* workspace;
+};
+
+// Launchers (return an attn_status_t value).
+int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
+size_t decode_workspace_bytes(int B, int Hq, int max_seqlen, int split, int d);
+
+}  // namespace attn

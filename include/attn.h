@@ -1,0 +1,177 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library libattn_gb300.so.
+ *
+ * The library computes exact scaled dot-product attention
+ *
+ *     O = softmax(Q K^T * scale + mask) V,     L = rowwise log-sum-exp of (Q K^T * scale + mask)
+ *
+ * in tiles with an online softmax, so the N x N score and probability matrices never reach
+ * device memory ("FlashAttention and GPU Data Movement", sections 2 and 3.1; "How
+ * FlashAttention Reduces HBM Traffic Exactly", section "FlashAttention's core move").
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named q, k, v, o, lse, k_cache, v_cache, cu_seqlens_k and workspace are DEVICE
+ *    pointers into memory the caller allocated and owns.  The library allocates no device
+ *    memory in any call and keeps no pointer after a call returns.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    Calls return without synchronising.  Results are valid once the stream reaches them.
+ *  - Tensors are contiguous, without strides.  Base pointers must be 16-byte aligned (the
+ *    tiles are moved by the Tensor Memory Accelerator).
+ *  - Element type: one `attn_dtype_t` applies to q, k, v and o alike.  Scores, the running
+ *    max and sum, and the output accumulator are fp32; O is rounded to the element type
+ *    (nearest-even); lse is fp32, natural log.
+ *  - Errors: argument errors return a negative `attn_status_t` before anything is launched.
+ *    A failed launch returns ATTN_ERR_LAUNCH.  Errors found on the device (a bounded wait that
+ *    timed out, a sequence length past the promised maximum) are latched in a per-device
+ *    status word that `attn_poll_status` returns.  There is no fallback path: an unsupported
+ *    shape or type is refused, never computed another way.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *attn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    ATTN_F16 = 0,  /* IEEE binary16 */
+    ATTN_BF16 = 1  /* bfloat16 */
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1, /* null pointer, negative size, Hq % Hkv != 0, bad scale ... */
+    ATTN_ERR_UNSUPPORTED = -2, /* valid request outside what the kernels implement (e.g. d)  */
+    ATTN_ERR_MISALIGNED = -3,  /* a base pointer is not 16-byte aligned                       */
+    ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than attn_decode_workspace_bytes */
+    ATTN_ERR_LAUNCH = -5,      /* the CUDA runtime refused a launch or a tensor map            */
+    ATTN_ERR_TIMEOUT = -6,     /* a bounded wait inside a kernel expired (device status word)  */
+    ATTN_ERR_DEVICE = -7,      /* no usable sm_103 device, or a device-side argument check     */
+    ATTN_ERR_BAD_LENGTHS = -8  /* device-side: a sequence is longer than max_seqlen_k or runs
+                                  past kv_capacity (its rows of o and lse are not written)     */
+} attn_status_t;
+
+/*
+ * attn_fwd -- exact attention forward (prefill), one fused kernel.
+ *
+ * Defined by: the three-step materialising definition S = Q K^T * scale, P = softmax(S),
+ * O = P V ("How FlashAttention Reduces HBM Traffic Exactly", section "The performance problem
+ * is data movement"), computed by the FA-2 loop -- one query tile per thread block, K/V tiles
+ * streamed through on-chip memory, online softmax with an unnormalised accumulator divided
+ * once at the end ("FlashAttention and GPU Data Movement", sections 2 and 3.1) -- with causal
+ * tiles past the diagonal skipped and the diagonal tiles masked (same page, section 2.1), and
+ * the log-sum-exp exported ("FlashAttention Explained", section "Why the statistics are cheap
+ * to store").
+ *
+ *   q   [B, Hq,  N_q,  d]  element type `dtype`
+ *   k   [B, Hkv, N_kv, d]
+ *   v   [B, Hkv, N_kv, d]
+ *   o   [B, Hq,  N_q,  d]  output, element type `dtype`
+ *   lse [B, Hq,  N_q]      output, fp32, L = m + ln(l) in units of the scaled scores;
+ *                          -inf for a row that sees no key
+ *   Grouped-query attention: query head h reads key/value head h / (Hq / Hkv).
+ *   causal != 0: key j is visible to query i iff j <= i + (N_kv - N_q) (bottom-right aligned;
+ *   plain "j <= i" when N_q == N_kv).  A row that sees no key gets O = 0 and L = -inf.
+ *   scale: multiplies the fp32 dot products (1/sqrt(d) in the usual case); must be finite
+ *   and > 0.
+ *
+ * Supported: d in {64, 128}; dtype F16 or BF16; Hq % Hkv == 0; B, Hq, Hkv >= 1;
+ * N_q, N_kv >= 0 (B == 0 or N_q == 0 is a no-op; N_kv == 0 gives O = 0, L = -inf).
+ * Returns ATTN_OK or a negative attn_status_t.  Requires one sm_103 GPU (tcgen05 tensor cores).
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int N_q, int N_kv, int d, int causal, float scale, attn_stream_t stream,
+             attn_dtype_t dtype);
+
+/*
+ * attn_decode_workspace_bytes -- device workspace attn_decode_splitkv needs.
+ *
+ * The split-KV decode writes one partial state (m, l, o[d]) per (sequence, query head,
+ * split) before merging them; this returns the bytes for B sequences of at most
+ * max_seqlen_k tokens cut into split_size-token splits.  Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_size, int d);
+
+/*
+ * attn_decode_splitkv -- one decode step: one new query token per sequence against its
+ * whole KV cache, split along the keys and merged exactly.
+ *
+ * Defined by: the same attention definition with a 1 x n score row ("FlashAttention and Why
+ * Attention Is a Memory-Traffic Problem", section "Prefill versus decode"); the key/value
+ * sequence is split into split_size-token chunks, each chunk produces a partial state
+ * (m, l, o) with the online softmax, and the partial states are merged with the block-merge
+ * rule m = max(m1, m2), l = e^(m1-m) l1 + e^(m2-m) l2, o = (e^(m1-m) l1 o1 + e^(m2-m) l2 o2)/l
+ * ("How FlashAttention Reduces HBM Traffic Exactly", section "Why softmax does not prevent
+ * tiling"; "FlashAttention Explained", section "Decoding, Paged and Split-KV Variants";
+ * "FlashAttention and GPU Data Movement", section 6.1).
+ *
+ *   q            [B, Hq, d]                  element type `dtype`
+ *   k_cache      [kv_capacity, Hkv, d]       packed (varlen) cache: sequence b owns token rows
+ *   v_cache      [kv_capacity, Hkv, d]       cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1
+ *   cu_seqlens_k [B + 1] int32, DEVICE, non-decreasing, cu_seqlens_k[0] = 0 is not required
+ *   kv_capacity  token rows allocated in each cache
+ *   max_seqlen_k upper bound on every sequence length (sizes the grid and the workspace);
+ *                a longer sequence is reported as ATTN_ERR_BAD_LENGTHS by attn_poll_status
+ *   o            [B, Hq, d] output, element type `dtype`
+ *   lse          [B, Hq] output fp32 (natural log, scaled scores); -inf for an empty sequence
+ *   split_size   tokens per split: a multiple of 64 in [64, 8192] (512 in the usual case)
+ *   workspace    device scratch of at least attn_decode_workspace_bytes(B, Hq, max_seqlen_k,
+ *                split_size, d) bytes, 16-byte aligned; its contents need no initialisation
+ *   Query head h reads key/value head h / (Hq / Hkv); Hq / Hkv must be <= 16.
+ *
+ * Supported: d in {64, 128}; dtype F16 or BF16.  Returns ATTN_OK or a negative attn_status_t.
+ * Calls that share a workspace must not overlap on the device.
+ */
+int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *cu_seqlens_k, int kv_capacity, int max_seqlen_k,
+                        void *o, float *lse, int B, int Hq, int Hkv, int d, int split_size,
+                        float scale, attn_dtype_t dtype, void *workspace,
+                        size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_poll_status -- synchronise `stream`, then read and clear the status word of the
+ * current device.  Returns ATTN_OK, the first device-side error latched since the last poll
+ * (ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_LENGTHS), or ATTN_ERR_LAUNCH if the synchronisation failed.
+ */
+int attn_poll_status(attn_stream_t stream);
+
+/* attn_status_string -- static text for a status code. */
+const char *attn_status_string(int status);
+
+/*
+ * attn_fwd_kv_tiles -- host-side copy of the tile range the prefill kernel walks for one
+ * query tile (the causal skip bound and the first tile needing the element mask, "FlashAttention
+ * and GPU Data Movement", section 2.1), exposed so the schedule can be checked without a GPU.
+ *
+ *   q_tile   0-based query tile (rows q_tile*block_m .. q_tile*block_m + block_m - 1)
+ *   block_m, block_n   query rows per tile, keys per K/V tile (the kernel uses 128, 128)
+ *   *n_tiles       number of K/V tiles loaded (tiles 0 .. n_tiles-1)
+ *   *first_masked  first K/V tile that needs the element mask (causal diagonal or the ragged
+ *                  end of the keys); == *n_tiles when none does
+ * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_kv_tiles(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
+                      int *n_tiles, int *first_masked);
+
+/*
+ * attn_selftest_timeout -- launch one tiny kernel that waits on a barrier nothing ever
+ * arrives at, with a limit of `limit_us` microseconds (1 .. 1000000), then records
+ * ATTN_ERR_TIMEOUT in the status word and returns.  Used to check, on a GPU, that a wait which
+ * runs out leaves the context usable and reports through attn_poll_status.
+ */
+int attn_selftest_timeout(int limit_us, attn_stream_t stream);
+
+/* attn_version -- library version string. */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

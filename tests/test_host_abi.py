@@ -1,0 +1,157 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every declared symbol, refuses bad
+arguments before any launch, and its host-side schedule helper reproduces the pages' causal
+tile listing.  No compute call is made (there is no GPU here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import __graft_entry__
+
+    __graft_entry__._cuda_build_module().build()
+    import exact_io_aware_09_gb300 as m
+
+    return m
+
+
+def _has_cuda():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def declared_functions():
+    txt = open(os.path.join(ROOT, "include", "attn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(attn_[a-z0-9_]+)\s*\(",
+                       txt, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes",
+                     "attn_poll_status", "attn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(attn):
+    lib = ctypes.CDLL(attn.library_path)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/attn.h but not exported"
+    assert "sm_103a" in attn.attn_version()
+
+
+def test_status_strings(attn):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        s = attn.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert attn.attn_status_string(123) == "unknown status"
+
+
+def test_kv_tile_range_matches_page_exercise(golden, attn):
+    g = golden("causal_tiles_ex4.json")
+    # the page's tiles are 1-based with B_r = 128, B_c = 64
+    n, fm = attn.attn_fwd_kv_tiles(g["query_tile"] - 1, g["Br"], g["Bc"], g["N"], g["N"], True)
+    assert n == len(g["loaded"]) and n == g["loaded"][-1]
+    assert fm == len(g["unmasked"])          # tiles 1..8 unmasked, 9 and 10 masked
+
+
+@pytest.mark.parametrize("bm,bn", [(128, 64), (128, 128), (64, 128), (128, 32)])
+@pytest.mark.parametrize("N", [1, 63, 128, 129, 500, 1024, 4096])
+def test_kv_tile_range_matches_oracle_listing(attn, bm, bn, N):
+    nq = -(-N // bm)
+    for qt in range(nq):
+        t = oracle.causal_tiles(qt + 1, bm, bn, N)
+        n, fm = attn.attn_fwd_kv_tiles(qt, bm, bn, N, N, True)
+        assert n == len(t["loaded"])
+        # the kernel also masks the ragged last K/V tile (keys past N), which the page's
+        # listing never meets because its N is a multiple of both tile sizes
+        ragged_last = (-(-N // bn) - 1) if N % bn else n
+        assert fm == min(len(t["unmasked"]), ragged_last)
+        n, fm = attn.attn_fwd_kv_tiles(qt, bm, bn, N, N, False)
+        assert n == -(-N // bn)
+        assert fm == (n - 1 if N % bn else n)
+
+
+def brute_tiles(qt, bm, bn, nq, nkv, causal):
+    """Tiles holding at least one (row, key) pair the mask keeps, and the first tile where some
+    row of the query tile loses a key to the mask or to the ragged end."""
+    rows = range(qt * bm, min((qt + 1) * bm, nq))
+    n_all = -(-nkv // bn)
+    vis = lambda i, j: j < nkv and (not causal or j <= i + nkv - nq)
+    loaded = [j for j in range(n_all) if any(vis(i, c) for i in rows for c in range(j * bn, (j + 1) * bn))]
+    n = (loaded[-1] + 1) if loaded else 0
+    first = n
+    for j in range(n):
+        if any(not vis(i, c) for i in rows for c in range(j * bn, (j + 1) * bn)):
+            first = j
+            break
+    return n, first
+
+
+@pytest.mark.parametrize("nq,nkv", [(5, 17), (17, 5), (64, 64), (70, 200), (200, 70), (1, 300),
+                                    (300, 1), (130, 130)])
+def test_kv_tile_range_bottom_right_brute_force(attn, nq, nkv):
+    bm, bn = 32, 16
+    for causal in (False, True):
+        for qt in range(-(-nq // bm)):
+            assert attn.attn_fwd_kv_tiles(qt, bm, bn, nq, nkv, causal) == brute_tiles(qt, bm, bn, nq, nkv, causal)
+
+
+def test_workspace_bytes(attn):
+    # (m, l) + o[d] fp32 per (sequence, head, split), o block padded to 256 bytes
+    parts = 64 * 64 * 64
+    assert attn.attn_decode_workspace_bytes(64, 64, 32768, 512, 128) == parts * 128 * 4 + parts * 8
+    assert attn.attn_decode_workspace_bytes(0, 64, 32768, 512, 128) == 0
+    assert attn.attn_decode_workspace_bytes(1, 1, 1, 512, 64) >= 66 * 4
+
+
+def test_bad_arguments_are_refused_before_launch(attn):
+    L = attn.lib
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails its checks
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    nul = ctypes.c_void_p(0)
+    s = 0.125
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 6, 4, 8, 8, 64, 0, s, nul, 0) == -1  # Hq % Hkv
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 8, 8, 96, 0, s, nul, 0) == -2  # d
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, -1.0, nul, 0) == -1
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, float("nan"), nul, 0) == -1
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, s, nul, 7) == -1  # dtype
+    assert L.attn_fwd(nul, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, s, nul, 0) == -1
+    assert L.attn_fwd(odd, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, s, nul, 0) == -3
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 0, 4, 4, 8, 8, 64, 0, s, nul, 0) == 0   # no-op
+    assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 0, 8, 64, 0, s, nul, 0) == 0
+    # A valid request with fake pointers must never reach a device: only where there is none
+    # is it checked that the call is refused (not computed some other way).
+    no_device = not _has_cuda()
+    if no_device:
+        assert L.attn_fwd(fake, fake, fake, fake, fake, 1, 4, 4, 8, 8, 64, 0, s, nul, 0) == -7
+
+    def dec(split=512, hq=64, hkv=8, d=128, ws_bytes=1 << 30, ws=fake, cu=fake):
+        return L.attn_decode_splitkv(fake, fake, fake, cu, 1024, 1024, fake, fake, 2, hq, hkv, d,
+                                     split, s, 1, ws, ws_bytes, nul)
+
+    assert dec(split=500) == -2
+    assert dec(split=32) == -2
+    assert dec(hq=64, hkv=2) == -2            # 32 query heads per key/value head
+    assert dec(hq=12, hkv=8) == -1
+    assert dec(d=80) == -2
+    assert dec(ws_bytes=16) == -4
+    assert dec(ws=nul) == -4
+    assert dec(cu=ctypes.c_void_p((1 << 20) + 2)) == -3
+    if no_device:
+        assert dec() == -7
+    assert L.attn_selftest_timeout(0, nul) == -1
+    assert L.attn_selftest_timeout(2_000_000, nul) == -1

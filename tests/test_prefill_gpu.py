@@ -1,0 +1,140 @@
+"""GPU parity of the prefill kernel (attn_fwd through the C ABI) against the fp64 oracle.
+
+Small shapes cover several tiles, ragged query and key tails, bottom-right causal alignment,
+rows with no visible key, grouped-query heads, both head dimensions and both element types;
+the benchmark workloads run at full size (all rows, except the 8192-token GQA workload, whose
+rows are sampled).  Tolerances are those of tests/parity.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from parity import check_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import exact_io_aware_09_gb300 as m
+
+    return m
+
+
+def run_gpu(attn, cfg, q, k, v, sentinel=True):
+    import torch
+
+    qt, kt, vt = (syn.bits_to_tensor(x, cfg.dtype, "cuda") for x in (q, k, v))
+    o = torch.full_like(qt, float("nan")) if sentinel else None
+    lse = torch.full((cfg.B, cfg.Hq, cfg.N_q), float("nan"), device="cuda") if sentinel else None
+    o, lse = attn.attn_fwd(qt, kt, vt, o=o, lse=lse, causal=cfg.causal, scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    return (o.float().cpu().numpy().astype(np.float64).reshape(-1, cfg.d),
+            lse.cpu().numpy().astype(np.float64).reshape(-1))
+
+
+def oracle_rows(cfg, q, k, v, rows=None):
+    return oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q, cfg.N_kv,
+                                 cfg.d, cfg.causal, cfg.scale, rows)
+
+
+SMALL = [
+    # (B, Hq, Hkv, N_q, N_kv, d, dtype, causal)
+    (1, 1, 1, 128, 128, 64, "f16", False),     # exactly one tile
+    (1, 1, 1, 256, 256, 64, "f16", False),     # the single-head workload
+    (1, 2, 2, 1, 1, 64, "bf16", False),        # one row, one key
+    (1, 2, 2, 1, 1, 128, "f16", True),
+    (2, 4, 2, 200, 333, 64, "bf16", True),     # ragged both ways, bottom-right causal
+    (2, 4, 2, 200, 333, 64, "bf16", False),
+    (1, 2, 1, 300, 300, 128, "f16", True),
+    (1, 4, 4, 129, 129, 128, "bf16", False),
+    (1, 2, 2, 1, 1000, 128, "bf16", True),     # one query row sees every key
+    (1, 2, 2, 400, 100, 64, "f16", True),      # N_kv < N_q: top rows see no key
+    (1, 3, 1, 517, 517, 128, "bf16", True),    # 3 query heads per key/value head
+    (1, 8, 1, 384, 384, 64, "f16", True),      # 8 query heads per key/value head
+    (2, 2, 2, 640, 640, 128, "f16", False),
+    (1, 2, 2, 1000, 1000, 128, "bf16", True),
+    (1, 1, 1, 255, 4000, 64, "bf16", False),   # long key side, short query side
+    (1, 1, 1, 4000, 255, 128, "f16", True),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(attn, shape):
+    B, Hq, Hkv, Nq, Nkv, d, dt, causal = shape
+    cfg = syn.PrefillConfig("small", B, Hq, Hkv, Nq, Nkv, d, dt, causal, 100 + sum(shape[:6]))
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, f"shape {shape}")
+
+
+def test_large_logits_small(attn):
+    cfg = syn.PrefillConfig("x8", 1, 2, 2, 300, 300, 128, "f16", True, 31, q_scale_pow2=3)
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, "x8 logits")
+
+
+def test_no_keys_and_empty_inputs(attn):
+    import torch
+
+    q = torch.randn(1, 2, 70, 64, device="cuda").half()
+    k = torch.empty(1, 2, 0, 64, device="cuda").half()
+    o, lse = attn.attn_fwd(q, k, k.clone(), causal=False)
+    assert attn.attn_poll_status() == 0
+    assert torch.all(o == 0) and torch.all(lse == float("-inf"))
+    q0 = torch.empty(1, 2, 0, 64, device="cuda").half()
+    o0, l0 = attn.attn_fwd(q0, q0, q0)
+    assert o0.numel() == 0 and l0.numel() == 0
+
+
+def test_stream_argument_is_honoured(attn):
+    import torch
+
+    cfg = syn.PrefillConfig("stream", 1, 2, 2, 256, 256, 64, "bf16", True, 5)
+    q, k, v = cfg.host_inputs()
+    s = torch.cuda.Stream()
+    qt, kt, vt = (syn.bits_to_tensor(x, cfg.dtype, "cuda") for x in (q, k, v))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        o, lse = attn.attn_fwd(qt, kt, vt, causal=True, scale=cfg.scale, stream=s)
+    s.synchronize()
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(o.float().cpu().numpy().reshape(-1, 64), lse.cpu().numpy().reshape(-1), orf, lrf,
+               "side stream")
+
+
+@pytest.mark.parametrize("cfg", [syn.CONFIG1, syn.CONFIG2], ids=lambda c: c.name)
+def test_workload_full(attn, cfg):
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, cfg.name)
+
+
+@pytest.mark.parametrize("cfg", [syn.CONFIG3A, syn.CONFIG3B, syn.CONFIG3SA, syn.CONFIG3SB],
+                         ids=lambda c: c.name)
+def test_long_workload_full(attn, cfg):
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, cfg.name)
+
+
+def test_gqa_long_context_sampled(attn):
+    cfg = syn.CONFIG4
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    rng = np.random.default_rng(4)
+    n = cfg.B * cfg.Hq * cfg.N_q
+    rows = np.unique(np.concatenate([
+        rng.integers(0, n, 6000),
+        # first and last rows of every head, and the rows around a tile boundary
+        np.arange(cfg.Hq) * cfg.N_q, np.arange(cfg.Hq) * cfg.N_q + cfg.N_q - 1,
+        np.arange(120, 140), cfg.N_q * 37 + np.arange(8000, 8192)])).astype(np.int64)
+    orf, lrf = oracle_rows(cfg, q, k, v, rows)
+    check_rows(og[rows], lg[rows], orf, lrf, cfg.name)
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
