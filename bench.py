@@ -242,6 +242,12 @@ def run_ours(args):
 
     pcfg = syn.CONFIG4
     dcfg = syn.CONFIG5
+    if args.decode_batch != dcfg.B:
+        lens = tuple(int(x) for x in dcfg.lengths()[: args.decode_batch])
+        dcfg = syn.DecodeConfig(f"{dcfg.name}_first{args.decode_batch}", args.decode_batch, dcfg.Hq,
+                                dcfg.Hkv, dcfg.d, dcfg.dtype, dcfg.seed, lengths_override=lens)
+    do_pre = args.only in ("both", "prefill")
+    do_dec = args.only in ("both", "decode")
     q, k, v = pcfg.device_inputs(device)
     o = torch.empty_like(q)
     lse = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), device=device, dtype=torch.float32)
@@ -256,11 +262,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def prefill():
-        attn.attn_fwd(q, k, v, o=o, lse=lse, causal=True, scale=pcfg.scale, stream=stream)
+        if do_pre:
+            attn.attn_fwd(q, k, v, o=o, lse=lse, causal=True, scale=pcfg.scale, stream=stream)
 
     def decode():
-        attn.attn_decode_splitkv(dq, dk, dv, cu, max_len, o=do, lse=dl, split_size=dcfg.split,
-                                 scale=dcfg.scale, workspace=ws, stream=stream)
+        if do_dec:
+            attn.attn_decode_splitkv(dq, dk, dv, cu, max_len, o=do, lse=dl, split_size=dcfg.split,
+                                     scale=dcfg.scale, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         prefill()
@@ -300,24 +308,25 @@ def run_ours(args):
     flops = pcfg.flops()
     kv_bytes = dcfg.kv_bytes()
     dec_bytes = kv_bytes + 2 * dq.numel() * 2 + dl.numel() * 4
-    value = flops * args.steps * world / (pre_ms_max / 1e3) / 1e12
-    dec_gbs = dec_bytes * args.steps * world / (dec_ms_max / 1e3) / 1e9
+    tiny = 1e-9
+    value = flops * args.steps * world / (max(pre_ms_max, tiny) / 1e3) / 1e12 if do_pre else None
+    dec_gbs = dec_bytes * args.steps * world / (max(dec_ms_max, tiny) / 1e3) / 1e9 if do_dec else None
     # per-launch rooflines of this rank's kernels
-    pre_launch_s = pre_ms / args.steps / 1e3
-    dec_launch_s = dec_ms / args.steps / 1e3
-    ach_t = flops / pre_launch_s / 1e12
-    ach_b = dec_bytes / dec_launch_s / 1e9
+    pre_launch_s = max(pre_ms, tiny) / args.steps / 1e3
+    dec_launch_s = max(dec_ms, tiny) / args.steps / 1e3
+    ach_t = flops / pre_launch_s / 1e12 if do_pre else 0.0
+    ach_b = dec_bytes / dec_launch_s / 1e9 if do_dec else 0.0
 
     # end to end through the public API with host buffers: H2D inputs, call, D2H result
-    e2e = run_e2e(args, attn, pcfg, q, k, v, stream, device, world)
+    e2e = run_e2e(args, attn, pcfg, q, k, v, stream, device, world) if (do_pre and not args.no_e2e) else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and do_pre and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pcfg, q, k, v)
 
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(value, 2) if value is not None else None,
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -350,7 +359,7 @@ def run_ours(args):
             "algorithmic_bytes": int((2 * q.numel() + 2 * k.numel()) * 2 + lse.numel() * 4),
         },
         "decode": {
-            "value": round(dec_gbs, 1),
+            "value": round(dec_gbs, 1) if dec_gbs is not None else None,
             "unit": "GB/s",
             "ms_per_launch": round(dec_ms / args.steps, 4),
             "roofline": {
@@ -367,7 +376,7 @@ def run_ours(args):
         },
         "prefill_ms_per_launch": round(pre_ms / args.steps, 4),
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
         "clocks": clocks,
         "wall_s_timed": round(wall_max, 4),
     }
@@ -502,6 +511,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["both", "prefill", "decode"], default="both",
+                    help="run one half of the step (for profiling)")
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="sequences of the decode workload (first B of the seeded lengths)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
