@@ -13,6 +13,7 @@ import os
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes",
+    "attn_decode_splitkv_static", "attn_decode_static_scratch_bytes",
     "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_selftest_timeout",
     "attn_version", "library_path", "lib",
 ]
@@ -38,6 +39,11 @@ lib.attn_decode_workspace_bytes.restype = _SZ
 lib.attn_decode_splitkv.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                                     _P, _SZ, _P]
 lib.attn_decode_splitkv.restype = _I
+lib.attn_decode_splitkv_static.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I,
+                                           _F, _I, _P]
+lib.attn_decode_splitkv_static.restype = _I
+lib.attn_decode_static_scratch_bytes.argtypes = []
+lib.attn_decode_static_scratch_bytes.restype = _SZ
 lib.attn_poll_status.argtypes = [_P]
 lib.attn_poll_status.restype = _I
 lib.attn_status_string.argtypes = [_I]
@@ -160,6 +166,43 @@ def attn_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, max_seqlen_k: int, o=
                                  _dev_ptr(workspace, "workspace"), workspace.numel(),
                                  _stream_handle(stream))
     _check(st, "attn_decode_splitkv")
+    return o, lse
+
+
+def attn_decode_static_scratch_bytes() -> int:
+    return int(lib.attn_decode_static_scratch_bytes())
+
+
+def attn_decode_splitkv_static(q, k_cache, v_cache, cu_seqlens_k, max_seqlen_k: int, o=None,
+                               lse=None, split_size: int = 512, scale: float | None = None,
+                               stream=None):
+    """attn_decode_splitkv without a workspace, for callers that cannot allocate device memory
+    during a decode step.
+
+    The partial states go to a fixed 32 MiB scratch array owned by the library (one per GPU,
+    kept until exit); requests needing more raise AttnError(ATTN_ERR_WORKSPACE).  All calls
+    share that array, so calls must not overlap on the GPU.  The first call on each GPU looks
+    the array up; make it before any stream capture.  ``o`` and ``lse`` are allocated here only
+    when omitted -- pass them to keep the call allocation-free.
+    """
+    torch = _torch()
+    B, Hq, d = q.shape
+    cap, Hkv, _ = k_cache.shape
+    if cu_seqlens_k.dtype != torch.int32 or cu_seqlens_k.numel() != B + 1:
+        raise AttnError(-1, "attn_decode_splitkv_static: cu_seqlens_k must be int32 [B+1]")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib.attn_decode_splitkv_static(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+                                        _dev_ptr(v_cache, "v_cache"),
+                                        _dev_ptr(cu_seqlens_k, "cu_seqlens_k"), cap,
+                                        int(max_seqlen_k), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"),
+                                        B, Hq, Hkv, d, int(split_size), float(scale),
+                                        _dtype_code(q), _stream_handle(stream))
+    _check(st, "attn_decode_splitkv_static")
     return o, lse
 
 

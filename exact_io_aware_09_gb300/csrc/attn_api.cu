@@ -151,6 +151,41 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   return launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_decode_splitkv_static(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* cu_seqlens_k, int kv_capacity, int max_seqlen_k,
+                               void* o, float* lse, int B, int Hq, int Hkv, int d, int split_size,
+                               float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  // Same checks as attn_decode_splitkv, except that the partial states go to the library's own
+  // fixed scratch instead of a caller workspace.  Nothing here allocates.
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || kv_capacity < 0 || max_seqlen_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!q || !o || !lse || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+  if (max_seqlen_k > 0 && kv_capacity > 0 && (!k_cache || !v_cache)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
+  if (need > attn_decode_static_scratch_bytes()) return ATTN_ERR_WORKSPACE;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  const int st = static_decode_scratch(&scratch, &scratch_bytes);
+  if (st != 0) return st;
+  if (need > scratch_bytes) return ATTN_ERR_WORKSPACE;
+  DecodeArgs a{q, k_cache, v_cache, cu_seqlens_k, kv_capacity, max_seqlen_k, o, lse, B,
+               Hq, Hkv, d, split_size, scale, dtype == ATTN_BF16, scratch};
+  return launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_static_scratch_bytes(void) { return size_t(32) << 20; }
+
 int attn_poll_status(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_LAUNCH;

@@ -16,6 +16,8 @@
 // to 16 rows) straight from the swizzled stage buffers.  The four warps' states are merged in
 // shared memory and the chunk's normalised (m, l, o) is written to the workspace.
 // Kernel 2 (merge): one block per (sequence, query head) merges that row's chunk states.
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -388,6 +390,39 @@ static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
   dim3 mgrid(a.Hq, a.B);
   attn_decode_merge_kernel<D, BF16><<<mgrid, D, 0, stream>>>(p, static_cast<uint16_t*>(a.o), a.lse);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+// ------------------------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand the decode a workspace: a serving loop that may not call
+// cudaMalloc in its step (the call can synchronise the whole device), a host that runs under a
+// fixed device-memory budget owned by another allocator it has no handle to, or an embedding
+// that lends the library only its input and output buffers.  For them the partial states live
+// in this fixed array, which every GPU that loads the library keeps until the process exits.  All calls share it: two such
+// calls running at the same time on the GPU would overwrite each other's partial states, so
+// they must be ordered (same stream, or synchronised).  Nothing in it needs to start at zero:
+// every partial state is written before it is read.
+// ------------------------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+int static_decode_scratch(void** ptr, size_t* bytes) {
+  static void* per_device[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -7;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!per_device[dev]) {
+    // Host code cannot use g_decode_scratch as a device address; ask the runtime for this
+    // device's copy (first call on each device, with that device current).
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return -5;
+    per_device[dev] = p;
+  }
+  *ptr = per_device[dev];
+  *bytes = kStaticScratchBytes;
+  return 0;
 }
 
 int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {

@@ -77,5 +77,8 @@ struct DecodeArgs {
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Hq, int max_seqlen, int split, int d);
+// Device address and size of the library-owned decode scratch of the current device
+// (set up on the first call per device).  Returns 0 or an attn_status_t value.
+int static_decode_scratch(void** ptr, size_t* bytes);
 
 }  // namespace attn

@@ -135,6 +135,38 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
                         size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_splitkv_static -- attn_decode_splitkv for callers that cannot allocate.
+ *
+ * No counterpart on the pages: this is a library convenience.  Some callers cannot obtain
+ * device memory at the point where they decode -- a serving loop that may not call cudaMalloc
+ * inside its step (the call can synchronise the whole device), a process whose device memory
+ * belongs to another allocator it has no handle to, or an embedding that lends the library only
+ * its input and output buffers.  This
+ * entry point takes the same inputs and outputs as attn_decode_splitkv (see there) but no
+ * workspace: the partial states go to a fixed scratch array inside the library, allocated once
+ * per GPU when the library is loaded and kept until the process exits.  The call itself
+ * allocates nothing.
+ *
+ *  - Limit: attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d) must not exceed
+ *    attn_decode_static_scratch_bytes() (32 MiB, e.g. 16 sequences x 64 heads x 32k tokens at
+ *    512-token splits, d = 128); larger requests return ATTN_ERR_WORKSPACE before any launch.
+ *  - The first call on each device looks up that device's copy of the scratch array (with the
+ *    device current); make that first call before any stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents.  Nothing in it
+ *    needs to start at zero, but two calls that overlap on the GPU (different streams without
+ *    ordering, or two threads) race on it: order them.
+ * Returns ATTN_OK or a negative attn_status_t.
+ */
+int attn_decode_splitkv_static(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *cu_seqlens_k, int kv_capacity, int max_seqlen_k,
+                               void *o, float *lse, int B, int Hq, int Hkv, int d,
+                               int split_size, float scale, attn_dtype_t dtype,
+                               attn_stream_t stream);
+
+/* attn_decode_static_scratch_bytes -- size of the scratch attn_decode_splitkv_static uses. */
+size_t attn_decode_static_scratch_bytes(void);
+
+/*
  * attn_poll_status -- synchronise `stream`, then read and clear the status word of the
  * current device.  Returns ATTN_OK, the first device-side error latched since the last poll
  * (ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_LENGTHS), or ATTN_ERR_LAUNCH if the synchronisation failed.
