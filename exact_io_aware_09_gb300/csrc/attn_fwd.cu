@@ -5,7 +5,7 @@
 // tiles of the matching key/value head through shared memory and keeps the online-softmax
 // state on chip, writing O and the log-sum-exp once at the end.
 //
-// Roles inside a thread block (192 threads):
+// Roles inside a thread block (224 threads):
 //   warps 0-3  softmax: thread r owns query row r.  Reads S_j from tensor memory, applies the
 //              scale, the causal/ragged mask and the online-softmax update ("FlashAttention and
 //              GPU Data Movement", section 3.1), writes P_j back to tensor memory as 16-bit
@@ -13,11 +13,13 @@
 //              epilogue O = a / l, L = m + ln l.
 //   warp 4     TMA producers: lane 0 loads Q once and K_j into a STAGES-deep ring, lane 1
 //              loads V_j into its own ring.
-//   warp 5     tcgen05 issuer: S_j = Q K_j^T (both operands in shared memory) and
-//              O += P_j V_j (P from tensor memory, V from shared memory), fp32 accumulators in
-//              tensor memory; allocates and frees the 512 tensor-memory columns.
+//   warp 5     tcgen05 issuer of S_j = Q K_j^T (both operands in shared memory, fp32 result in
+//              tensor memory); allocates and frees the 512 tensor-memory columns.
+//   warp 6     tcgen05 issuer of O += P_j V_j (P from tensor memory, V from shared memory, fp32
+//              accumulator in tensor memory).
 // Tensor memory: S buffers at columns 0 and 128 (double-buffered so Q K_{j+1}^T runs while the
-// softmax of tile j runs), the output accumulator at column 256.
+// softmax of tile j runs), the output accumulator at column 256, two P buffers after it.  A
+// softmax releases its S buffer as soon as it has read it, so the score MMAs run ahead.
 //
 // Departures from the pages' kernels (prior art for A100/H100/B200): accumulators live in tensor
 // memory instead of registers, P is handed to the second MMA through tensor memory instead of
@@ -32,12 +34,36 @@
 
 namespace attn {
 
+// Optional per-tile timestamps for schedule analysis; compiled in only when ATTN_FWD_TRACE is
+// defined (never in the library build).
+#ifdef ATTN_FWD_TRACE
+__device__ unsigned long long g_fwd_trace[8][80][16];
+#define FWD_TRACE(j, ev)                                                                      \
+  do {                                                                                        \
+    if (trace_slot >= 0 && (j) < 80) {                                                        \
+      unsigned long long t_;                                                                  \
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t_));                                      \
+      g_fwd_trace[trace_slot][(j)][(ev)] = t_;                                                \
+    }                                                                                         \
+  } while (0)
+#else
+#define FWD_TRACE(j, ev) \
+  do {                   \
+  } while (0)
+#endif
+
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 224;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// P buffers follow O: columns 256 + d and 256 + d + 64 (16-bit pairs, 64 columns each).
+template <int D>
+struct PCols {
+  static constexpr uint32_t kP0 = kColO + D, kP1 = kColO + D + 64;
+  static_assert(kP1 + 64 <= kTmemCols, "tensor memory budget");
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max rises by > 2^8
 constexpr uint32_t kSubTile = 128 * 128;   // bytes of one 64-column, 128-row swizzled sub-tile
 constexpr uint64_t kDrainLimitNs = 100000000ull;
@@ -58,8 +84,9 @@ struct FwdLayout {
   static constexpr uint32_t kK = kQ + kQBytes;
   static constexpr uint32_t kV = kK + STAGES * kKVBytes;
   static constexpr uint32_t kBar = kV + STAGES * kKVBytes;
-  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_ready, o_done, drain
-  static constexpr uint32_t kNumBars = 1 + 4 * STAGES + 2 + 3;
+  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], s_free[2], p_ready[2],
+  // o_done[2], drain  (the [2] barriers belong to the two S and the two P buffers)
+  static constexpr uint32_t kNumBars = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;   // + alignment slack
 };
@@ -92,9 +119,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #define BAR_KE(s) (bars + 8u * (1u + 2u * STAGES + (s)))
 #define BAR_VE(s) (bars + 8u * (1u + 3u * STAGES + (s)))
 #define BAR_S(b) (bars + 8u * (1u + 4u * STAGES + (b)))
-  const uint32_t bar_p = bars + 8u * (3u + 4u * STAGES);
-  const uint32_t bar_o = bars + 8u * (4u + 4u * STAGES);
-  const uint32_t bar_drain = bars + 8u * (5u + 4u * STAGES);
+#define BAR_SF(b) (bars + 8u * (3u + 4u * STAGES + (b)))
+#define BAR_P(b) (bars + 8u * (5u + 4u * STAGES + (b)))
+#define BAR_O(b) (bars + 8u * (7u + 4u * STAGES + (b)))
+  const uint32_t bar_drain = bars + 8u * (9u + 4u * STAGES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
 
@@ -111,7 +139,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int q0 = qt * kBlockM;
   int n_tiles, first_masked;
   kv_tile_range(qt, kBlockM, kBlockN, p.N_q, p.N_kv, p.causal, n_tiles, first_masked);
+#ifdef ATTN_FWD_TRACE
+  int trace_slot = -1;
+  {
+    const int ids[8] = {0, 1, 2, 3, 600, 1200, 2000, 4000};
+    for (int i = 0; i < 8; ++i)
+      if (static_cast<int>(blockIdx.x) == ids[i]) trace_slot = i;
+  }
+#endif
 
+  if (threadIdx.x == 0) FWD_TRACE(79, 0);
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < STAGES; ++s) {
@@ -122,9 +159,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(BAR_S(0), 1);
     mbar_init(BAR_S(1), 1);
-    mbar_init(bar_p, kSoftmaxThreads);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(BAR_SF(0), kSoftmaxThreads);
+    mbar_init(BAR_SF(1), kSoftmaxThreads);
+    mbar_init(BAR_P(0), kSoftmaxThreads);
+    mbar_init(BAR_P(1), kSoftmaxThreads);
+    mbar_init(BAR_O(0), 1);
+    mbar_init(BAR_O(1), 1);
+    mbar_init(bar_drain, 2);  // one commit from each issuer
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -175,40 +216,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         wait_bounded(is_k ? BAR_K(j % STAGES) : BAR_V(j % STAGES), (j / STAGES) & 1, nullptr,
                      p.status, kDrainLimitNs);
     }
-  } else if (warp == 5) {
-    // ----------------------------------------------------------------- tcgen05 issuer
+  } else if (warp == 5 || warp == 6) {
+    // ----------------------------------------------------------------- tcgen05 issuers
+    // Warp 5 issues the score MMAs, warp 6 the P V MMAs.  The two streams touch disjoint tensor
+    // memory (S buffers / O and P buffers) and disjoint shared memory (Q, K / V), so they need no
+    // ordering between them beyond the barriers below, and each issuer's waits overlap the other
+    // issuer's MMAs.
     if (lane == 0 && n_tiles > 0) {
+      const bool qk_issuer = (warp == 5);
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
-      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status);
-      // O += P_t V_t for tile t (P_t in the S buffer of tile t, V_t in ring slot t % STAGES).
-      auto issue_pv = [&](int t) -> bool {
-        if (!wait_bounded(bar_p, t & 1, abort_flag, p.status)) return false;
+      bool ok = qk_issuer ? wait_bounded(bar_q, 0, abort_flag, p.status) : true;
+      // S_t = Q K_t^T into S buffer t % 2, once the softmax of tile t - 2 has read that buffer.
+      auto issue_qk = [&](int t) -> bool {
+        FWD_TRACE(t, 8);
         const int s = t % STAGES;
-        if (!wait_bounded(BAR_V(s), (t / STAGES) & 1, abort_flag, p.status)) return false;
+        if (t >= 2 && !wait_bounded(BAR_SF(t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status))
+          return false;
+        if (!wait_bounded(BAR_K(s), (t / STAGES) & 1, abort_flag, p.status)) return false;
+        FWD_TRACE(t, 9);
         tc_fence_after();
-        const uint32_t p_col = tmem + ((t & 1) ? kColS1 : kColS0);
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          // V is [keys, d] with d contiguous: the B operand is MN-major.  16 keys per MMA
-          // (two 8-row groups, SBO = 1024 B apart); the two 64-column halves of d are
-          // separate swizzled sub-tiles (LBO = one sub-tile).
-          const uint64_t bdesc = make_sdesc_sw128(sV + s * L::kKVBytes + kk * 16 * 128,
-                                                  kSubTile, 1024);
-          mma_ts(tmem + kColO, p_col + kk * 8, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar_o);
-        mma_commit(BAR_VE(s));  // V slot free
-        return true;
-      };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % STAGES;
-        if (!wait_bounded(BAR_K(s), (j / STAGES) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t s_col = tmem + ((j & 1) ? kColS1 : kColS0);
+        const uint32_t s_col = tmem + ((t & 1) ? kColS1 : kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // Q and K are K-major (d contiguous): 16 elements = 32 bytes per MMA inside the
@@ -218,11 +246,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint64_t bdesc = make_sdesc_sw128(sK + s * L::kKVBytes + off, 16, 1024);
           mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(BAR_S(j & 1));
+        mma_commit(BAR_S(t & 1));
         mma_commit(BAR_KE(s));  // K slot free
-        if (j > 0 && !issue_pv(j - 1)) ok = false;
-      }
-      if (ok) issue_pv(n_tiles - 1);
+        FWD_TRACE(t, 10);
+        return true;
+      };
+      // O += P_t V_t (P_t in P buffer t % 2, V_t in ring slot t % STAGES).
+      auto issue_pv = [&](int t) -> bool {
+        FWD_TRACE(t, 11);
+        if (!wait_bounded(BAR_P(t & 1), (t >> 1) & 1, abort_flag, p.status)) return false;
+        FWD_TRACE(t, 12);
+        const int s = t % STAGES;
+        if (!wait_bounded(BAR_V(s), (t / STAGES) & 1, abort_flag, p.status)) return false;
+        FWD_TRACE(t, 13);
+        tc_fence_after();
+        const uint32_t p_col = tmem + ((t & 1) ? PCols<D>::kP1 : PCols<D>::kP0);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          // V is [keys, d] with d contiguous: the B operand is MN-major.  16 keys per MMA
+          // (two 8-row groups, SBO = 1024 B apart); the two 64-column halves of d are
+          // separate swizzled sub-tiles (LBO = one sub-tile).
+          const uint64_t bdesc = make_sdesc_sw128(sV + s * L::kKVBytes + kk * 16 * 128,
+                                                  kSubTile, 1024);
+          mma_ts(tmem + kColO, p_col + kk * 8, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(BAR_O(t & 1));
+        mma_commit(BAR_VE(s));  // V slot free
+        FWD_TRACE(t, 14);
+        return true;
+      };
+      // The score issuer runs up to two tiles ahead of the softmax (two S buffers); the P V
+      // issuer follows the softmax tile by tile.
+      for (int j = 0; ok && j < n_tiles; ++j) ok = qk_issuer ? issue_qk(j) : issue_pv(j);
       // Every MMA this thread issued completes before the block frees tensor memory.
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kDrainLimitNs);
@@ -238,17 +293,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float m = -INFINITY;  // running max of the scaled scores, log2 units
     float l = 0.0f;       // running sum of 2^(x - m)
     bool ok = true;
+    bool s_ready = false;  // S_j already seen complete by an early test during tile j - 1
     for (int j = 0; j < n_tiles; ++j) {
       const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
-      if (!warp_wait(BAR_S(j & 1), (j >> 1) & 1, abort_flag, p.status)) {
+      if (r == 0) FWD_TRACE(j, 0);
+      if (!__all_sync(0xffffffffu, s_ready) &&
+          !warp_wait(BAR_S(j & 1), (j >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
+      if (r == 0) FWD_TRACE(j, 1);
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(row_tmem + s_col + c * 32, sr[c]);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(BAR_SF(j & 1));  // S buffer free for Q K_{j+2}^T
+      if (r == 0) FWD_TRACE(j, 2);
+      // Early, non-blocking tests of the two barriers this tile and the next will need; their
+      // latency hides under the exponentials below.
+      const bool p_free = (j < 2) || mbar_test_wait(BAR_O(j & 1), ((j >> 1) - 1) & 1);
       float x[kBlockN];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -262,16 +327,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c > rel) x[c] = -INFINITY;
       }
+      // Row maximum: three-input max, eight independent chains.
       float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = x[e];
+      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(x[e], x[8 + e]);
 #pragma unroll
-      for (int c = 8; c < kBlockN; c += 8)
+      for (int c = 16; c < kBlockN; c += 16)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], x[c + e]);
-      const float tile_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int e = 0; e < 8; ++e) mx[e] = max3f(mx[e], x[c + e], x[c + 8 + e]);
+      const float tile_max = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m, tile_max * sl2);
       float alpha = 1.0f;
       if (m_new - m > kRescaleThreshold) {  // also true for the first finite maximum
@@ -279,45 +344,63 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m = m_new;
       }
       const float neg_mu = (m == -INFINITY) ? 0.0f : -m;
+      // p = 2^(x * scale * log2(e) - m): one packed FMA per pair of scores, MUFU ex2, a packed
+      // add into four pair-accumulators for the row sum, and the 16-bit pack for P.
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < kBlockN; c += 2) {
-        const float p0 = ex2(fmaf(x[c], sl2, neg_mu));
-        const float p1 = ex2(fmaf(x[c + 1], sl2, neg_mu));
-        ps[(c >> 1) & 7] += p0 + p1;
+        float a0, a1;
+        fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_mu, neg_mu);
+        const float p0 = ex2(a0);
+        const float p1 = ex2(a1);
+        const int k2 = ((c >> 1) & 3) * 2;
+        add2(ps[k2], ps[k2 + 1], p0, p1);
         pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
       }
       l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
-      tmem_st32(row_tmem + s_col, pk[0]);
-      tmem_st32(row_tmem + s_col + 32, pk[1]);
-      if (j > 0) {
-        // The previous P V has to finish before the accumulator is touched (and before this
-        // tile's P is published, which keeps the p_ready phases in step with the issuer).
-        if (!warp_wait(bar_o, (j - 1) & 1, abort_flag, p.status)) {
+      s_ready = (j + 1 < n_tiles) && mbar_test_wait(BAR_S((j + 1) & 1), ((j + 1) >> 1) & 1);
+      if (r == 0) FWD_TRACE(j, 3);
+      // P buffer j % 2 was last read by P V_{j-2}: it has to be done before P_j overwrites it.
+      if (j >= 2) {
+        if (!__all_sync(0xffffffffu, p_free) &&
+            !warp_wait(BAR_O(j & 1), ((j >> 1) - 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // order the P store after the MMA that read the buffer
+      }
+      if (r == 0) FWD_TRACE(j, 4);
+      const uint32_t p_col = (j & 1) ? PCols<D>::kP1 : PCols<D>::kP0;
+      tmem_st32(row_tmem + p_col, pk[0]);
+      tmem_st32(row_tmem + p_col + 32, pk[1]);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // Rescaling the accumulator needs P V_{j-1} finished; P V_j waits for this tile's
+        // p_ready, so nothing else touches O meanwhile.
+        if (!warp_wait(BAR_O((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(row_tmem + kColO + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(row_tmem + kColO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(row_tmem + kColO + c * 32, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(row_tmem + kColO + c * 32, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(BAR_P(j & 1));
+      if (r == 0) FWD_TRACE(j, 5);
     }
     // ------------------------------------------------------------- epilogue
     if (ok && n_tiles > 0) {
-      ok = warp_wait(bar_o, (n_tiles - 1) & 1, abort_flag, p.status);
+      // MMAs complete in issue order: the last P V done means every MMA is done.
+      ok = warp_wait(BAR_O((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag, p.status);
       tc_fence_after();
     }
     const bool have = ok && n_tiles > 0;
@@ -366,8 +449,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #undef BAR_KE
 #undef BAR_VE
 #undef BAR_S
+#undef BAR_SF
+#undef BAR_P
+#undef BAR_O
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) FWD_TRACE(79, 1);
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -415,6 +502,14 @@ static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
   kern<<<static_cast<unsigned>(blocks), kFwdThreads, L::kBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
+
+#ifdef ATTN_FWD_TRACE
+}  // namespace attn
+extern "C" int attn_fwd_trace_copy(void* dst) {
+  return static_cast<int>(cudaMemcpyFromSymbol(dst, attn::g_fwd_trace, sizeof(attn::g_fwd_trace)));
+}
+namespace attn {
+#endif
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (a.B == 0 || a.N_q == 0) return 0;
