@@ -76,14 +76,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with parity `parity` of barrier `bar` has completed.  Gives up when
-// `*abort` becomes non-zero (another role already timed out) or after `limit_ns`; on a
-// time-out it sets *abort and latches ATTN_ERR_TIMEOUT.  Returns true when the phase completed.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                             int* status, uint64_t limit_ns = kWaitLimitNs) {
-#pragma unroll 1
-  for (int i = 0; i < 32; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of wait_bounded: spin with try_wait until the phase completes, `*abort` becomes
+// non-zero (another role already timed out) or `limit_ns` passes; on a time-out it sets *abort
+// and latches ATTN_ERR_TIMEOUT.  Kept out of line so the common case stays a single try_wait.
+static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               int* status, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
   while (true) {
@@ -95,6 +92,14 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
       return false;
     }
   }
+}
+
+// Wait until the phase with parity `parity` of barrier `bar` has completed, with the bound and
+// abort rules of wait_bounded_slow.  Returns true when the phase completed.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             int* status, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, abort, status, limit_ns);
 }
 
 // ------------------------------------------------------------------------------------------
