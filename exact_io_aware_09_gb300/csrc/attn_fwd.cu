@@ -5,17 +5,18 @@
 // tiles of the matching key/value head through shared memory and keeps the online-softmax
 // state on chip, writing O and the log-sum-exp once at the end.
 //
-// Roles inside a thread block (224 threads):
-//   warps 0-3  softmax: thread r owns query row r.  Reads S_j from tensor memory, applies the
-//              scale, the causal/ragged mask and the online-softmax update ("FlashAttention and
-//              GPU Data Movement", section 3.1), writes P_j back to tensor memory as 16-bit
-//              pairs, rescales the accumulator when the row maximum moved, and runs the
-//              epilogue O = a / l, L = m + ln l.
-//   warp 4     TMA producers: lane 0 loads Q once and K_j into a STAGES-deep ring, lane 1
-//              loads V_j into its own ring.
-//   warp 5     tcgen05 issuer of S_j = Q K_j^T (both operands in shared memory, fp32 result in
+// Roles inside a thread block (384 threads):
+//   warps 0-7  softmax, two warpgroups taking alternate K/V tiles (0-3 the even ones, 4-7 the
+//              odd ones); thread r of a warpgroup owns query row r.  Reads S_j from tensor
+//              memory, applies the scale, the causal/ragged mask and the online-softmax update
+//              ("FlashAttention and GPU Data Movement", section 3.1), writes P_j back to tensor
+//              memory as 16-bit pairs, rescales the accumulator when the row maximum moved, and
+//              runs the epilogue O = a / l, L = m + ln l (each warpgroup half of the columns).
+//   warp 8     TMA producer: Q once, then K_j into a STAGES-deep ring.
+//   warp 11    TMA producer: V_j into its own STAGES-deep ring.
+//   warp 9     tcgen05 issuer of S_j = Q K_j^T (both operands in shared memory, fp32 result in
 //              tensor memory); allocates and frees the 512 tensor-memory columns.
-//   warp 6     tcgen05 issuer of O += P_j V_j (P from tensor memory, V from shared memory, fp32
+//   warp 10    tcgen05 issuer of O += P_j V_j (P from tensor memory, V from shared memory, fp32
 //              accumulator in tensor memory).
 // Tensor memory: S buffers at columns 0 and 128 (double-buffered so Q K_{j+1}^T runs while the
 // softmax of tile j runs), the output accumulator at column 256, two P buffers after it.  A
@@ -54,8 +55,9 @@ __device__ unsigned long long g_fwd_trace[8][80][16];
 
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kFwdThreads = 224;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kFwdThreads = 384;  // warps 0-7 softmax, 8 and 11 TMA, 9-10 MMA issue
+constexpr int kSoftmaxThreads = 128;  // one softmax warpgroup (thread = query row)
+constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kVProducerWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 // P buffers follow O: columns 256 + d and 256 + d + 64 (16-bit pairs, 64 columns each).
@@ -85,10 +87,16 @@ struct FwdLayout {
   static constexpr uint32_t kV = kK + STAGES * kKVBytes;
   static constexpr uint32_t kBar = kV + STAGES * kKVBytes;
   // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], s_free[2], p_ready[2],
-  // o_done[2], drain  (the [2] barriers belong to the two S and the two P buffers)
-  static constexpr uint32_t kNumBars = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
+  // o_done[2], drain, m_ready[2]  (the [2] barriers belong to the two S and P buffers, i.e.
+  // to the even and the odd tiles)
+  static constexpr uint32_t kNumBars = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1 + 2;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr uint32_t kBytes = kMisc + 16 + 1024;   // + alignment slack
+  // running row maxima handed from one softmax warpgroup to the other: [tile parity][row], and
+  // the odd warpgroup's row sums for the epilogue: [row]
+  static constexpr uint32_t kMrow = kMisc + 16;
+  static constexpr uint32_t kLsum = kMrow + 2 * kBlockM * 4;
+  static constexpr uint32_t kBytes = kLsum + kBlockM * 4 + 1024;  // + alignment slack
+  static_assert(kBytes <= 232448, "shared memory per block");
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -123,6 +131,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #define BAR_P(b) (bars + 8u * (5u + 4u * STAGES + (b)))
 #define BAR_O(b) (bars + 8u * (7u + 4u * STAGES + (b)))
   const uint32_t bar_drain = bars + 8u * (9u + 4u * STAGES);
+#define BAR_M(b) (bars + 8u * (10u + 4u * STAGES + (b)))
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
 
@@ -166,10 +175,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(BAR_O(0), 1);
     mbar_init(BAR_O(1), 1);
     mbar_init(bar_drain, 2);  // one commit from each issuer
+    mbar_init(BAR_M(0), kSoftmaxThreads);
+    mbar_init(BAR_M(1), kSoftmaxThreads);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kQkWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -178,12 +189,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
     // ----------------------------------------------------------------- TMA producers
-    // Lane 0 loads Q and the K ring, lane 1 the V ring: a K slot is refilled as soon as its
-    // Q K^T finished, a V slot once its P V finished, without one ring waiting on the other.
-    if (lane < 2 && n_tiles > 0) {
-      const bool is_k = (lane == 0);
+    // Warp 8 loads Q and the K ring, warp 11 the V ring (separate warps, so neither waits on
+    // the other's spin): a K slot is refilled as soon as its Q K^T finished, a V slot once its
+    // P V finished.
+    if (lane == 0 && n_tiles > 0) {
+      const bool is_k = (warp == kProducerWarp);
       const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
       const uint32_t ring = is_k ? sK : sV;
       if (is_k) {
@@ -216,14 +228,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         wait_bounded(is_k ? BAR_K(j % STAGES) : BAR_V(j % STAGES), (j / STAGES) & 1, nullptr,
                      p.status, kDrainLimitNs);
     }
-  } else if (warp == 5 || warp == 6) {
+  } else if (warp == kQkWarp || warp == kPvWarp) {
     // ----------------------------------------------------------------- tcgen05 issuers
     // Warp 5 issues the score MMAs, warp 6 the P V MMAs.  The two streams touch disjoint tensor
     // memory (S buffers / O and P buffers) and disjoint shared memory (Q, K / V), so they need no
     // ordering between them beyond the barriers below, and each issuer's waits overlap the other
     // issuer's MMAs.
     if (lane == 0 && n_tiles > 0) {
-      const bool qk_issuer = (warp == 5);
+      const bool qk_issuer = (warp == kQkWarp);
       constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
       constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
       bool ok = qk_issuer ? wait_bounded(bar_q, 0, abort_flag, p.status) : true;
@@ -285,35 +297,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------------------- softmax + epilogue
-    const int r = threadIdx.x;  // query row inside the tile; lane quarter = warp
-    const uint32_t row_tmem = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // Two warpgroups share the rows: warps 0-3 take the even K/V tiles (S0, P0), warps 4-7 the
+    // odd ones (S1, P1); in both, thread r owns query row r and warp % 4 is its tensor-memory
+    // lane quarter.  The running maximum is the only state carried from tile to tile: the
+    // warpgroup of tile j publishes m_j as soon as its row maxima are known (BAR_M), and the
+    // other warpgroup, on tile j + 1, waits for it before its exponentials.  Each warpgroup keeps
+    // its own partial row sum, rescaled whenever the maximum moves; the two are added at the end.
+    const int wg = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const bool tracer = (threadIdx.x & 127) == 0;
+    const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int row = q0 + r;
     const int off = p.N_kv - p.N_q;
     const float sl2 = p.sl2;
-    float m = -INFINITY;  // running max of the scaled scores, log2 units
-    float l = 0.0f;       // running sum of 2^(x - m)
+    float* mrow = reinterpret_cast<float*>(gbase + L::kMrow);  // [tile parity][row]
+    float* lsum = reinterpret_cast<float*>(gbase + L::kLsum);  // [row]
+    const uint32_t s_col = wg ? kColS1 : kColS0;
+    const uint32_t p_col = wg ? PCols<D>::kP1 : PCols<D>::kP0;
+    float m_own = -INFINITY;  // maximum (log2 units) this warpgroup's partial sum refers to
+    float l = 0.0f;           // this warpgroup's partial sum of 2^(x - m_own)
     bool ok = true;
-    bool s_ready = false;  // S_j already seen complete by an early test during tile j - 1
-    for (int j = 0; j < n_tiles; ++j) {
-      const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
-      if (r == 0) FWD_TRACE(j, 0);
+    bool s_ready = false;  // S of this warpgroup's next tile already seen complete
+    for (int j = wg; j < n_tiles; j += 2) {
+      const int u = j >> 1;  // use index of this warpgroup's S and P buffers
+      if (tracer) FWD_TRACE(j, 0);
       if (!__all_sync(0xffffffffu, s_ready) &&
-          !warp_wait(BAR_S(j & 1), (j >> 1) & 1, abort_flag, p.status)) {
+          !warp_wait(BAR_S(wg), u & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
-      if (r == 0) FWD_TRACE(j, 1);
+      if (tracer) FWD_TRACE(j, 1);
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(row_tmem + s_col + c * 32, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(BAR_SF(j & 1));  // S buffer free for Q K_{j+2}^T
-      if (r == 0) FWD_TRACE(j, 2);
-      // Early, non-blocking tests of the two barriers this tile and the next will need; their
-      // latency hides under the exponentials below.
-      const bool p_free = (j < 2) || mbar_test_wait(BAR_O(j & 1), ((j >> 1) - 1) & 1);
+      mbar_arrive(BAR_SF(wg));  // S buffer free for Q K_{j+2}^T
+      if (tracer) FWD_TRACE(j, 2);
+      // Early, non-blocking test of the barrier needed before P is written (P V_{j-2} read
+      // this P buffer); its latency hides under the work below.
+      const bool p_free = (j < 2) || mbar_test_wait(BAR_O(wg), (u - 1) & 1);
       float x[kBlockN];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -327,7 +352,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c > rel) x[c] = -INFINITY;
       }
-      // Row maximum: three-input max, eight independent chains.
+      // Row maximum of the tile: three-input max, eight independent chains.
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = fmaxf(x[e], x[8 + e]);
@@ -337,13 +362,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int e = 0; e < 8; ++e) mx[e] = max3f(mx[e], x[c + e], x[c + 8 + e]);
       const float tile_max = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
                                    fmaxf(mx[6], mx[7]));
-      const float m_new = fmaxf(m, tile_max * sl2);
-      float alpha = 1.0f;
-      if (m_new - m > kRescaleThreshold) {  // also true for the first finite maximum
-        alpha = ex2(m - m_new);
-        m = m_new;
+      // Running maximum after tile j - 1, from the other warpgroup.
+      float m_prev = -INFINITY;
+      if (j > 0) {
+        if (!warp_wait(BAR_M(wg ^ 1), ((j - 1) >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        m_prev = mrow[(wg ^ 1) * kBlockM + r];
       }
-      const float neg_mu = (m == -INFINITY) ? 0.0f : -m;
+      // The maximum moves only when it rises by more than 2^8 (also for the first finite one).
+      float m_j = m_prev;
+      float alpha = 1.0f;  // rescale of the accumulator O for this tile
+      const float m_new = fmaxf(m_prev, tile_max * sl2);
+      if (m_new - m_prev > kRescaleThreshold) {
+        alpha = ex2(m_prev - m_new);
+        m_j = m_new;
+      }
+      mrow[wg * kBlockM + r] = m_j;
+      mbar_arrive(BAR_M(wg));  // m_j published for tile j + 1
+      if (m_j != m_own) {
+        l = (m_own == -INFINITY) ? 0.0f : l * ex2(m_own - m_j);
+        m_own = m_j;
+      }
+      const float neg_mu = (m_j == -INFINITY) ? 0.0f : -m_j;
       // p = 2^(x * scale * log2(e) - m): one packed FMA per pair of scores, MUFU ex2, a packed
       // add into four pair-accumulators for the row sum, and the 16-bit pack for P.
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -358,26 +400,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         add2(ps[k2], ps[k2 + 1], p0, p1);
         pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
       }
-      l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
-      s_ready = (j + 1 < n_tiles) && mbar_test_wait(BAR_S((j + 1) & 1), ((j + 1) >> 1) & 1);
-      if (r == 0) FWD_TRACE(j, 3);
-      // P buffer j % 2 was last read by P V_{j-2}: it has to be done before P_j overwrites it.
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      s_ready = (j + 2 < n_tiles) && mbar_test_wait(BAR_S(wg), (u + 1) & 1);
+      if (tracer) FWD_TRACE(j, 3);
       if (j >= 2) {
         if (!__all_sync(0xffffffffu, p_free) &&
-            !warp_wait(BAR_O(j & 1), ((j >> 1) - 1) & 1, abort_flag, p.status)) {
+            !warp_wait(BAR_O(wg), (u - 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();  // order the P store after the MMA that read the buffer
       }
-      if (r == 0) FWD_TRACE(j, 4);
-      const uint32_t p_col = (j & 1) ? PCols<D>::kP1 : PCols<D>::kP0;
+      if (tracer) FWD_TRACE(j, 4);
       tmem_st32(row_tmem + p_col, pk[0]);
       tmem_st32(row_tmem + p_col + 32, pk[1]);
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // Rescaling the accumulator needs P V_{j-1} finished; P V_j waits for this tile's
-        // p_ready, so nothing else touches O meanwhile.
-        if (!warp_wait(BAR_O((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.status)) {
+        // p_ready and P V_{j+1} comes after it, so nothing else touches O meanwhile.
+        if (!warp_wait(BAR_O(wg ^ 1), ((j - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -394,22 +434,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(BAR_P(j & 1));
-      if (r == 0) FWD_TRACE(j, 5);
+      mbar_arrive(BAR_P(wg));
+      if (tracer) FWD_TRACE(j, 5);
     }
     // ------------------------------------------------------------- epilogue
+    // The final maximum is the one after the last tile; the warpgroup that did not process
+    // that tile reads it from the exchange.
+    const int last = n_tiles - 1;
+    float m_fin = m_own;
+    if (ok && n_tiles > 0 && (last & 1) != wg) {
+      if (warp_wait(BAR_M(last & 1), (last >> 1) & 1, abort_flag, p.status))
+        m_fin = mrow[(last & 1) * kBlockM + r];
+      else
+        ok = false;
+    }
     if (ok && n_tiles > 0) {
       // MMAs complete in issue order: the last P V done means every MMA is done.
-      ok = warp_wait(BAR_O((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag, p.status);
+      ok = warp_wait(BAR_O(last & 1), (last >> 1) & 1, abort_flag, p.status);
       tc_fence_after();
     }
+    // Both partial sums onto the final maximum, then added (the odd warpgroup's through lsum,
+    // the total handed back through mrow once nobody reads the maxima any more).
+    if (m_own != m_fin) l = (m_own == -INFINITY) ? 0.0f : l * ex2(m_own - m_fin);
+    named_bar_sync(1, 2 * kSoftmaxThreads);
+    if (wg == 1) lsum[r] = l;
+    named_bar_sync(1, 2 * kSoftmaxThreads);
+    if (wg == 0) {
+      l += lsum[r];
+      mrow[r] = l;
+    }
+    named_bar_sync(1, 2 * kSoftmaxThreads);
+    const float l_row = (wg == 0) ? l : mrow[r];
     const bool have = ok && n_tiles > 0;
-    const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+    const float inv_l = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+    // Each warpgroup normalises and stores half of the output columns.
     if (have) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
-        tmem_ld32(row_tmem + kColO + c * 32, o);
+        tmem_ld32(row_tmem + kColO + wg * (D / 2) + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -418,30 +481,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           w.y = pack2<BF16>(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
           w.z = pack2<BF16>(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
           w.w = pack2<BF16>(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-          const uint32_t chunk = c * 4 + q4;  // 16-byte chunk of the row (8 elements)
+          const uint32_t chunk = wg * (D / 16) + c * 4 + q4;  // 16-byte chunk of the row
           uint8_t* dst = gbase + L::kQ + (chunk >> 3) * kSubTile + sw128(r, chunk & 7);
           *reinterpret_cast<uint4*>(dst) = w;
         }
       }
     } else if (ok) {
       // No key visible to any row of this tile: O = 0.
-      for (int chunk = 0; chunk < D / 8; ++chunk) {
+      for (int c = 0; c < D / 16; ++c) {
+        const int chunk = wg * (D / 16) + c;
         uint8_t* dst = gbase + L::kQ + (chunk >> 3) * kSubTile + sw128(r, chunk & 7);
         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
       }
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, kSoftmaxThreads);
-    if (ok && r == 0 && *abort_flag == 0) {
+    named_bar_sync(1, 2 * kSoftmaxThreads);
+    if (ok && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_o, sQ + sub * kSubTile, sub * 64, q0, bh);
       tma_store_commit();
       tma_store_wait_read0();
     }
-    if (ok && row < p.N_q) {
-      const float mu = (m == -INFINITY) ? 0.0f : m;
+    if (ok && wg == 0 && row < p.N_q) {
+      const float mu = (m_fin == -INFINITY) ? 0.0f : m_fin;
       p.lse[static_cast<size_t>(bh) * p.N_q + row] =
-          (l > 0.0f) ? (mu + lg2(l)) * 0.69314718055994531f : -INFINITY;
+          (l_row > 0.0f) ? (mu + lg2(l_row)) * 0.69314718055994531f : -INFINITY;
     }
   }
 #undef BAR_K
@@ -452,10 +516,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #undef BAR_SF
 #undef BAR_P
 #undef BAR_O
+#undef BAR_M
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) FWD_TRACE(79, 1);
-  if (warp == 5) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

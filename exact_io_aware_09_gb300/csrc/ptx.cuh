@@ -253,6 +253,19 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ------------------------------------------------------------------------------------------
+// register rebalancing between warpgroups (all threads of a warpgroup execute the same one)
+// ------------------------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------------------------------
 // named barriers
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
