@@ -78,8 +78,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Slow path of wait_bounded: spin with try_wait until the phase completes, `*abort` becomes
 // non-zero (another role already timed out) or `limit_ns` passes; on a time-out it sets *abort
-// and latches ATTN_ERR_TIMEOUT.  Kept out of line so the common case stays a single try_wait.
-static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+// and latches ATTN_ERR_TIMEOUT.  Inlined: a kernel that rebalances registers between
+// warpgroups (setmaxnreg) cannot contain calls.
+static __device__ __forceinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int* abort,
                                                int* status, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
@@ -118,6 +119,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Pull a tile into L2 ahead of its TMA load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y,
                                              int z) {
   asm volatile(
@@ -133,6 +142,10 @@ __device__ __forceinline__ void tma_store_commit() {
 
 __device__ __forceinline__ void tma_store_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -253,7 +266,39 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ------------------------------------------------------------------------------------------
-// register rebalancing between warpgroups (all threads of a warpgroup execute the same one)
+// cluster launch control: a running block takes over the work of a block not yet launched
+// ------------------------------------------------------------------------------------------
+// Asks the hardware to cancel the launch of one pending block of this grid.  The 16-byte answer
+// is written to shared memory at `resp` (16-byte aligned) and completes 16 transaction bytes on
+// `bar` (the caller has armed it with arrive.expect_tx).  After one answer that reports no
+// cancellation, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Decodes an answer: true and the x index of the cancelled block, or false (nothing left).
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 v;\n\t"
+      "ld.shared.b128 v, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, v;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, v;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  ctaid_x = static_cast<int>(x);
+  return ok != 0;
+}
+
+// ------------------------------------------------------------------------------------------
+// register rebalancing between warpgroups (every warp of a warpgroup executes the same one)
 // ------------------------------------------------------------------------------------------
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {

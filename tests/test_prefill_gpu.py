@@ -59,6 +59,17 @@ SMALL = [
     (1, 1, 1, 4000, 255, 128, "f16", True),
 ]
 
+# More work items than SMs, so that every resident block runs several items back to back:
+# mixed item lengths, items with no visible key between the others, one-tile items (no partial
+# sum to hand over) and ragged query tiles.
+MANY_ITEMS = [
+    (2, 80, 16, 300, 100, 64, "bf16", True),   # a third of the items see no key
+    (1, 96, 8, 700, 700, 128, "f16", True),    # 1 to 6 K/V tiles per item
+    (4, 64, 64, 130, 130, 64, "bf16", False),  # two tiles each, every other item 2 rows
+    (2, 200, 50, 128, 64, 128, "bf16", False), # one tile each
+    (1, 160, 160, 257, 1000, 128, "bf16", True),
+]
+
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
 def test_small_shapes(attn, shape):
@@ -68,6 +79,35 @@ def test_small_shapes(attn, shape):
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
     check_rows(og, lg, orf, lrf, f"shape {shape}")
+
+
+@pytest.mark.parametrize("shape", MANY_ITEMS, ids=lambda s: "x".join(map(str, s)))
+def test_many_items(attn, shape):
+    B, Hq, Hkv, Nq, Nkv, d, dt, causal = shape
+    cfg = syn.PrefillConfig("items", B, Hq, Hkv, Nq, Nkv, d, dt, causal, 200 + sum(shape[:6]))
+    q, k, v = cfg.host_inputs()
+    og, lg = run_gpu(attn, cfg, q, k, v)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, f"shape {shape}")
+
+
+def test_output_16_byte_aligned(attn):
+    """O only 16-byte aligned (the API's minimum for every pointer)."""
+    import torch
+
+    cfg = syn.PrefillConfig("align", 1, 96, 8, 300, 300, 128, "bf16", True, 211)
+    q, k, v = cfg.host_inputs()
+    qt, kt, vt = (syn.bits_to_tensor(x, cfg.dtype, "cuda") for x in (q, k, v))
+    backing = torch.full((qt.numel() + 8,), float("nan"), device="cuda", dtype=qt.dtype)
+    o = backing[8:].view(qt.shape)
+    assert o.data_ptr() % 32 == 16
+    o, lse = attn.attn_fwd(qt, kt, vt, o=o, causal=True, scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    assert torch.isnan(backing[:8]).all()  # nothing written before O
+    og = o.float().cpu().numpy().astype(np.float64).reshape(-1, cfg.d)
+    lg = lse.cpu().numpy().astype(np.float64).reshape(-1)
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, "16-byte aligned O")
 
 
 def test_large_logits_small(attn):
