@@ -61,6 +61,9 @@ def _load():
         lib.oracle_attention_rows.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                               f64, P, i64, P, P, i32]
         lib.oracle_attention_rows.restype = i32
+        lib.oracle_attention_rows_masked.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                     i32, i64, P, i32, f64, P, i64, P, P, i32]
+        lib.oracle_attention_rows_masked.restype = i32
         lib.oracle_decode_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, i64,
                                            P, P, i32]
         lib.oracle_decode_rows.restype = i32
@@ -128,11 +131,13 @@ def bits_to_double(bits: np.ndarray, dtype) -> np.ndarray:
 # the definition
 # ----------------------------------------------------------------------------------------
 def attention_rows(q, k, v, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale, rows=None,
-                   threads: int = 0):
+                   threads: int = 0, window=None, block_mask=None, block: int = 128):
     """O and L of the materialising definition for selected query rows.
 
     q, k, v: uint16 bit arrays, shapes [B,Hq,Nq,d] and [B,Hkv,Nkv,d].
     rows: flat indices (b*Hq + h)*Nq + i; ``None`` = every row.
+    window: sliding window W (key j visible to row i iff 0 <= i + Nkv - Nq - j <= W), or None.
+    block_mask: [ceil(Nq/block), ceil(Nkv/block)] pattern of blocks to compute, or None.
     Returns (o [n_rows, d] float64, lse [n_rows] float64).
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -144,9 +149,14 @@ def attention_rows(q, k, v, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale, rows=N
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     o = np.zeros((len(rows), d), dtype=np.float64)
     lse = np.zeros(len(rows), dtype=np.float64)
-    rc = _load().oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), _DT[dtype], B, Hq, Hkv, Nq,
-                                       Nkv, d, int(bool(causal)), float(scale), _ptr(rows),
-                                       len(rows), _ptr(o), _ptr(lse), int(threads))
+    if block_mask is not None:
+        block_mask = np.ascontiguousarray(block_mask, dtype=np.uint8)
+        assert block_mask.shape == (-(-Nq // block), -(-Nkv // block)), block_mask.shape
+    rc = _load().oracle_attention_rows_masked(
+        _ptr(q), _ptr(k), _ptr(v), _DT[dtype], B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)),
+        -1 if window is None else int(window),
+        _ptr(block_mask) if block_mask is not None else None, int(block), float(scale),
+        _ptr(rows), len(rows), _ptr(o), _ptr(lse), int(threads))
     if rc != 0:
         raise ValueError("oracle_attention_rows: bad arguments")
     return o, lse

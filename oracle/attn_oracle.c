@@ -27,7 +27,14 @@
  *  - a row with no visible key has O = 0 and L = -inf;
  *  - decode is the same definition with one query row per (sequence, head) and the whole
  *    cache of that sequence visible ("FlashAttention and Why Attention Is a Memory-Traffic
- *    Problem", section "Prefill versus decode": S is 1 x n).
+ *    Problem", section "Prefill versus decode": S is 1 x n);
+ *  - the sliding window is the pages' sliding_causal mask ("FlashAttention Explained",
+ *    FlexAttention section: key kv is visible to query q iff q >= kv and q - kv <= W), with
+ *    the same bottom-right alignment: j is visible to i iff 0 <= (i + N_kv - N_q) - j <= W;
+ *  - a block-sparse pattern lists the (query block, key block) pairs to compute
+ *    ("FlashAttention, annotated", section 3.3; the BlockMask of "FlashAttention Explained"
+ *    with one pattern for every batch and head); keys outside listed blocks are invisible,
+ *    and inside a listed block the causal and window rules still apply.
  *
  * Besides the definition the file holds two small pieces of the method itself, written out
  * in the pages' order, so that the pages' worked traces can pin them:
@@ -180,12 +187,34 @@ static void softmax_pv_row_d(const double *s, double *p, int64_t n, const double
  * rows[r] = (b * Hq + h) * Nq + i selects query row i of head h of batch b.
  * Outputs: o[r * d + c] and lse[r] in fp64.  Returns 0, or -1 on bad arguments.
  */
+int oracle_attention_rows_masked(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 int dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                                 int causal, int64_t window, const uint8_t *block_mask,
+                                 int block, double scale, const int64_t *rows, int64_t n_rows,
+                                 double *o, double *lse, int n_threads);
+
 int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                           int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal,
                           double scale, const int64_t *rows, int64_t n_rows, double *o,
                           double *lse, int n_threads) {
+    return oracle_attention_rows_masked(q, k, v, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, -1, NULL,
+                                        0, scale, rows, n_rows, o, lse, n_threads);
+}
+
+/*
+ * The same with the two masks that change the operator: a sliding window of W keys behind
+ * the diagonal (window >= 0; -1 = none) and a block-sparse pattern block_mask
+ * [ceil(Nq / block)][ceil(Nkv / block)] (nonzero = compute; NULL = none).
+ */
+int oracle_attention_rows_masked(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 int dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                                 int causal, int64_t window, const uint8_t *block_mask,
+                                 int block, double scale, const int64_t *rows, int64_t n_rows,
+                                 double *o, double *lse, int n_threads) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nkv < 0 || d <= 0)
         return -1;
+    if (block_mask && block <= 0) return -1;
+    const int64_t n_kvb = block_mask ? ((int64_t)Nkv + block - 1) / block : 0;
     if (n_rows == 0) return 0;
     double *tab = make_table(dtype);
     if (!tab) return -1;
@@ -236,6 +265,14 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
             for (int64_t j = 0; j < Nkv; ++j) {
                 vr[j] = vp + j * d;
                 if (causal && j > i + off) { s[j] = -INFINITY; continue; }
+                if (window >= 0 && (j > i + off || i + off - j > window)) {
+                    s[j] = -INFINITY;
+                    continue;
+                }
+                if (block_mask && !block_mask[(i / block) * n_kvb + j / block]) {
+                    s[j] = -INFINITY;
+                    continue;
+                }
                 double acc = 0.0;
                 if (kd) {
                     const double *kr = kd + plane + j * d;

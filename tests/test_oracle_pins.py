@@ -447,3 +447,101 @@ def test_decode_definition_matches_prefill_and_direct():
                                       vx[t0:t0 + L].transpose(1, 0, 2)[None], False, cfg.scale, 8, 2)
             np.testing.assert_allclose(o[b * 8:(b + 1) * 8], od.reshape(8, 16), atol=1e-12)
             np.testing.assert_allclose(lse[b * 8:(b + 1) * 8], ld.reshape(8), atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------
+# the masks that change the operator: sliding window and block-sparse pattern
+# ("FlashAttention Explained", FlexAttention section, sliding_causal; "FlashAttention,
+# annotated", section 3.3)
+# ------------------------------------------------------------------------------------
+def _masked_inputs(B, Hq, Hkv, Nq, Nkv, d, seed, dtype=BF16):
+    cfg = syn.PrefillConfig("m", B, Hq, Hkv, Nq, Nkv, d, dtype, True, seed)
+    return cfg, cfg.host_inputs()
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(37, 37), (20, 45), (45, 20)])
+def test_window_wider_than_the_sequence_is_causal(Nq, Nkv):
+    cfg, (q, k, v) = _masked_inputs(1, 4, 2, Nq, Nkv, 16, 700 + Nq)
+    oc, lc = oracle.attention_rows(q, k, v, BF16, 1, 4, 2, Nq, Nkv, 16, True, cfg.scale)
+    for causal in (True, False):   # the window implies the causal bound either way
+        ow, lw = oracle.attention_rows(q, k, v, BF16, 1, 4, 2, Nq, Nkv, 16, causal, cfg.scale,
+                                       window=Nkv + Nq)
+        np.testing.assert_array_equal(ow, oc)
+        np.testing.assert_array_equal(lw, lc)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(33, 33), (12, 40), (40, 12)])
+def test_window_zero_sees_only_the_diagonal_key(Nq, Nkv):
+    """W = 0: one visible key per row, so O is that key's value row and L its score."""
+    cfg, (q, k, v) = _masked_inputs(1, 2, 1, Nq, Nkv, 8, 800 + Nq)
+    o, lse = oracle.attention_rows(q, k, v, BF16, 1, 2, 1, Nq, Nkv, 8, True, cfg.scale, window=0)
+    # bf16 -> fp32 by bit placement, independently of the oracle's conversion table
+    as_f64 = lambda bits: (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qx, kx, vx = as_f64(q), as_f64(k), as_f64(v)
+    off = Nkv - Nq
+    for h in range(2):
+        for i in range(Nq):
+            r = h * Nq + i
+            j = i + off
+            if j < 0:
+                assert lse[r] == -np.inf and np.all(o[r] == 0.0)
+                continue
+            np.testing.assert_array_equal(o[r], vx[0, 0, j])
+            assert abs(lse[r] - cfg.scale * float(np.dot(qx[0, h, i], kx[0, 0, j]))) < 1e-12
+
+
+@pytest.mark.parametrize("W", [1, 5, 16])
+def test_window_row_is_full_attention_over_its_keys(W):
+    """Each windowed row equals unmasked attention over the keys [i + off - W, i + off]."""
+    Nq, Nkv, d = 30, 41, 16
+    cfg, (q, k, v) = _masked_inputs(1, 2, 2, Nq, Nkv, d, 900 + W)
+    o, lse = oracle.attention_rows(q, k, v, BF16, 1, 2, 2, Nq, Nkv, d, True, cfg.scale, window=W)
+    off = Nkv - Nq
+    for h in range(2):
+        for i in range(Nq):
+            hi = i + off
+            lo = max(0, hi - W)
+            ks = np.ascontiguousarray(k[:, h:h + 1, lo:hi + 1])
+            vs = np.ascontiguousarray(v[:, h:h + 1, lo:hi + 1])
+            qs = np.ascontiguousarray(q[:, h:h + 1, i:i + 1])
+            of, lf = oracle.attention_rows(qs, ks, vs, BF16, 1, 1, 1, 1, hi - lo + 1, d, False,
+                                           cfg.scale)
+            np.testing.assert_allclose(o[h * Nq + i], of[0], rtol=0, atol=1e-14)
+            assert abs(lse[h * Nq + i] - lf[0]) < 1e-13
+
+
+def test_block_mask_all_ones_and_all_zeros():
+    Nq, Nkv, d, bs = 50, 70, 8, 16
+    cfg, (q, k, v) = _masked_inputs(1, 2, 1, Nq, Nkv, d, 950)
+    shape = (-(-Nq // bs), -(-Nkv // bs))
+    for causal in (False, True):
+        ref = oracle.attention_rows(q, k, v, BF16, 1, 2, 1, Nq, Nkv, d, causal, cfg.scale)
+        ones = oracle.attention_rows(q, k, v, BF16, 1, 2, 1, Nq, Nkv, d, causal, cfg.scale,
+                                     block_mask=np.ones(shape, np.uint8), block=bs)
+        np.testing.assert_array_equal(ones[0], ref[0])
+        np.testing.assert_array_equal(ones[1], ref[1])
+    o, lse = oracle.attention_rows(q, k, v, BF16, 1, 2, 1, Nq, Nkv, d, False, cfg.scale,
+                                   block_mask=np.zeros(shape, np.uint8), block=bs)
+    assert np.all(o == 0.0) and np.all(lse == -np.inf)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_row_is_full_attention_over_listed_blocks(causal):
+    Nq, Nkv, d, bs = 48, 64, 8, 8
+    cfg, (q, k, v) = _masked_inputs(1, 1, 1, Nq, Nkv, d, 960 + causal)
+    rng = np.random.default_rng(961)
+    mask = (rng.random((Nq // bs, Nkv // bs)) < 0.4).astype(np.uint8)
+    o, lse = oracle.attention_rows(q, k, v, BF16, 1, 1, 1, Nq, Nkv, d, causal, cfg.scale,
+                                   block_mask=mask, block=bs)
+    off = Nkv - Nq
+    for i in range(Nq):
+        keys = [j for j in range(Nkv) if mask[i // bs, j // bs] and (not causal or j <= i + off)]
+        if not keys:
+            assert lse[i] == -np.inf and np.all(o[i] == 0.0)
+            continue
+        ks = np.ascontiguousarray(k[:, :, keys])
+        vs = np.ascontiguousarray(v[:, :, keys])
+        qs = np.ascontiguousarray(q[:, :, i:i + 1])
+        of, lf = oracle.attention_rows(qs, ks, vs, BF16, 1, 1, 1, 1, len(keys), d, False, cfg.scale)
+        np.testing.assert_allclose(o[i], of[0], rtol=0, atol=1e-14)
+        assert abs(lse[i] - lf[0]) < 1e-13
