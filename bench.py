@@ -206,6 +206,39 @@ def row_flops(cfg, rows):
     return float(4.0 * cfg.d * np.clip(vis, 0, None).sum())
 
 
+def visible_keys_window(N_q, N_kv, W):
+    """Visible keys per query row under the sliding window (bottom-right aligned)."""
+    i = np.arange(N_q, dtype=np.int64)
+    hi = np.minimum(i + N_kv - N_q, N_kv - 1)
+    lo = np.maximum(i + N_kv - N_q - W, 0)
+    return np.clip(hi - lo + 1, 0, None)
+
+
+def visible_keys_blocks(N_q, N_kv, mask, causal, bs=128):
+    """Visible keys per query row under a block pattern (and the causal rule if set)."""
+    out = np.zeros(N_q, dtype=np.int64)
+    keys = np.arange(N_kv, dtype=np.int64)
+    for i in range(N_q):
+        vis = mask[i // bs][keys // bs] != 0
+        if causal:
+            vis &= keys <= i + N_kv - N_q
+        out[i] = int(vis.sum())
+    return out
+
+
+def variant_pattern(N_q, N_kv, seed=11):
+    """Block pattern of the block-sparse measurement: the causal blocks, each kept with
+    probability 1/2, plus the diagonal and the first key block of every query tile."""
+    nq, nk = -(-N_q // 128), -(-N_kv // 128)
+    rng = np.random.default_rng(seed)
+    m = (rng.random((nq, nk)) < 0.5).astype(np.uint8)
+    for r in range(nq):
+        m[r, r + 1:] = 0
+        m[r, min(r, nk - 1)] = 1
+        m[r, 0] = 1
+    return m
+
+
 def time_oracle_prefill(cfg, q, k, v, budget_s=12.0, rows_per_batch=64, seed=0):
     import oracle
 
@@ -320,6 +353,10 @@ def run_ours(args):
     # end to end through the public API with host buffers: H2D inputs, call, D2H result
     e2e = run_e2e(args, attn, pcfg, q, k, v, stream, device, world) if (do_pre and not args.no_e2e) else None
 
+    variants = None
+    if do_pre and not args.no_variants:
+        variants = measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
+
     cpu = None
     if rank == 0 and world == 1 and do_pre and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pcfg, q, k, v)
@@ -375,6 +412,7 @@ def run_ours(args):
             },
         },
         "prefill_ms_per_launch": round(pre_ms / args.steps, 4),
+        "variants": variants,
         "e2e": e2e,
         "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
         "clocks": clocks,
@@ -386,6 +424,55 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src):
+    """The prefill variants that change the operator, on the same inputs: the pages' sliding
+    window (W = 1024) and a block pattern.  TFLOP/s from the exact visible (query, key) pairs
+    (4*d FLOPs each); timed with CUDA events over args.steps launches after 3 warm-ups."""
+    import torch
+
+    W = 1024
+    pattern = variant_pattern(pcfg.N_q, pcfg.N_kv)
+    mask = torch.from_numpy(pattern).to(q.device)
+    per_head = {
+        "window": visible_keys_window(pcfg.N_q, pcfg.N_kv, W).sum(),
+        "block_sparse": visible_keys_blocks(pcfg.N_q, pcfg.N_kv, pattern, True).sum(),
+    }
+    calls = {
+        "window": lambda: attn.attn_fwd_window(q, k, v, W, o=o, lse=lse, scale=pcfg.scale,
+                                                stream=stream),
+        "block_sparse": lambda: attn.attn_fwd_block_sparse(q, k, v, mask, causal=True, o=o, lse=lse,
+                                                           scale=pcfg.scale, stream=stream),
+    }
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st = attn.attn_poll_status()
+        if st != 0:
+            raise SystemExit(f"device status after {name}: {attn.attn_status_string(st)}")
+        ms = e0.elapsed_time(e1) / args.steps
+        flops = 4.0 * pcfg.d * float(per_head[name]) * pcfg.B * pcfg.Hq
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {
+            "workload": (f"sliding window W={W}" if name == "window" else
+                         f"causal block pattern, {int(pattern.sum())} of {pattern.size} blocks")
+                        + " on the prefill workload's inputs",
+            "ms_per_launch": round(ms, 4), "flops_per_launch": flops, "value": round(tf, 1),
+            "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                         "frac": round(tf / peaks["bf16_tflops"], 4)},
+        }
+    return out
 
 
 def run_e2e(args, attn, pcfg, q, k, v, stream, device, world):
@@ -512,6 +599,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the sliding-window and block-sparse prefill measurements")
     ap.add_argument("--only", choices=["both", "prefill", "decode"], default="both",
                     help="run one half of the step (for profiling)")
     ap.add_argument("--decode-batch", type=int, default=64,

@@ -34,6 +34,11 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
 lib.attn_fwd.restype = _I
+lib.attn_fwd_window.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
+lib.attn_fwd_window.restype = _I
+lib.attn_fwd_block_sparse.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P,
+                                      _I]
+lib.attn_fwd_block_sparse.restype = _I
 lib.attn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
 lib.attn_decode_workspace_bytes.restype = _SZ
 lib.attn_decode_splitkv.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _F, _I,
@@ -50,6 +55,8 @@ lib.attn_status_string.argtypes = [_I]
 lib.attn_status_string.restype = ctypes.c_char_p
 lib.attn_fwd_kv_tiles.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
 lib.attn_fwd_kv_tiles.restype = _I
+lib.attn_fwd_kv_span.argtypes = [_I, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_I)] * 4
+lib.attn_fwd_kv_span.restype = _I
 lib.attn_selftest_timeout.argtypes = [_I, _P]
 lib.attn_selftest_timeout.restype = _I
 lib.attn_version.argtypes = []
@@ -130,6 +137,63 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | Non
                       float(scale), _stream_handle(stream), _dtype_code(q))
     _check(st, "attn_fwd")
     return o, lse
+
+
+def _fwd_prep(q, k, v, o, lse, scale):
+    torch = _torch()
+    B, Hq, N_q, d = q.shape
+    _, Hkv, N_kv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise AttnError(-1, "attn_fwd: q/k/v shapes or dtypes disagree")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N_q), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return B, Hq, Hkv, N_q, N_kv, d, o, lse, float(scale)
+
+
+def attn_fwd_window(q, k, v, window: int, o=None, lse=None, scale: float | None = None,
+                    stream=None):
+    """Sliding-window prefill: key j visible to row i iff 0 <= i + N_kv - N_q - j <= window.
+
+    Shapes and return value as attn_fwd.
+    """
+    B, Hq, Hkv, N_q, N_kv, d, o, lse, scale = _fwd_prep(q, k, v, o, lse, scale)
+    st = lib.attn_fwd_window(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                             _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(window), scale,
+                             _stream_handle(stream), _dtype_code(q))
+    _check(st, "attn_fwd_window")
+    return o, lse
+
+
+def attn_fwd_block_sparse(q, k, v, block_mask, causal: bool = False, o=None, lse=None,
+                          scale: float | None = None, stream=None):
+    """Block-sparse prefill.  block_mask: uint8 CUDA tensor [ceil(N_q/128), ceil(N_kv/128)],
+    nonzero = compute that (query tile, key tile) block.  Shapes and return value as attn_fwd.
+    """
+    torch = _torch()
+    B, Hq, Hkv, N_q, N_kv, d, o, lse, scale = _fwd_prep(q, k, v, o, lse, scale)
+    shape = ((N_q + 127) // 128, (N_kv + 127) // 128)
+    if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != shape
+            or not block_mask.is_contiguous()):
+        raise AttnError(-1, f"attn_fwd_block_sparse: block_mask must be contiguous uint8 {shape}")
+    st = lib.attn_fwd_block_sparse(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                   _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv,
+                                   d, int(bool(causal)), _dev_ptr(block_mask, "block_mask"), scale,
+                                   _stream_handle(stream), _dtype_code(q))
+    _check(st, "attn_fwd_block_sparse")
+    return o, lse
+
+
+def attn_fwd_kv_span(q_tile: int, block_m: int, block_n: int, N_q: int, N_kv: int,
+                     causal: bool, window: int = -1):
+    """(j_begin, j_end, lo_masked, hi_masked) of the prefill schedule for one query tile."""
+    out = [_I(0) for _ in range(4)]
+    _check(lib.attn_fwd_kv_span(q_tile, block_m, block_n, N_q, N_kv, int(bool(causal)),
+                                int(window), *[ctypes.byref(x) for x in out]), "attn_fwd_kv_span")
+    return tuple(x.value for x in out)
 
 
 def attn_decode_workspace_bytes(B: int, Hq: int, max_seqlen_k: int, split_size: int, d: int) -> int:

@@ -101,9 +101,11 @@ using namespace attn;
 
 extern "C" {
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-             int Hkv, int N_q, int N_kv, int d, int causal, float scale, attn_stream_t stream,
-             attn_dtype_t dtype) {
+// The three prefill entry points share their checks and the kernel.
+static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int N_q, int N_kv, int d, int causal, int window,
+                      const uint8_t* block_mask, float scale, attn_stream_t stream,
+                      attn_dtype_t dtype) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || N_q < 0 || N_kv < 0 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
@@ -116,8 +118,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return ATTN_ERR_MISALIGNED;
   const int dev_ok = check_device();
   if (dev_ok != ATTN_OK) return dev_ok;
-  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale, dtype == ATTN_BF16};
+  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale,
+            dtype == ATTN_BF16, window, block_mask};
   return launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N_q, int N_kv, int d, int causal, float scale, attn_stream_t stream,
+             attn_dtype_t dtype) {
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal, -1, nullptr, scale,
+                    stream, dtype);
+}
+
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int Hq, int Hkv, int N_q, int N_kv, int d, int window, float scale,
+                    attn_stream_t stream, attn_dtype_t dtype) {
+  if (window < 0) return ATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, 1, window, nullptr, scale,
+                    stream, dtype);
+}
+
+int attn_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int N_q, int N_kv, int d, int causal,
+                          const uint8_t* block_mask, float scale, attn_stream_t stream,
+                          attn_dtype_t dtype) {
+  if (!block_mask) return ATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal, -1, block_mask, scale,
+                    stream, dtype);
+}
+
+int attn_fwd_kv_span(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
+                     int window, int* j_begin, int* j_end, int* lo_masked, int* hi_masked) {
+  if (q_tile < 0 || block_m <= 0 || block_n <= 0 || N_q < 0 || N_kv < 0 || window < -1 ||
+      !j_begin || !j_end || !lo_masked || !hi_masked)
+    return ATTN_ERR_INVALID_ARG;
+  kv_tile_span(q_tile, block_m, block_n, N_q, N_kv, causal ? 1 : 0, window, *j_begin, *j_end,
+               *lo_masked, *hi_masked);
+  return ATTN_OK;
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_size, int d) {

@@ -93,6 +93,9 @@ struct FwdParams {
   int n_qtiles, group, causal;
   int BH;           // batch * Hq
   int head_group;   // query heads walked together, longest query tiles first (see decode_item)
+  int window;       // sliding window, keys behind the diagonal (-1: none)
+  int n_kvtiles;    // key tiles of the sequence (row length of block_mask)
+  const uint8_t* block_mask;  // [query tile][key tile], nonzero = compute; null: every tile
   float sl2;  // scale * log2(e)
 };
 
@@ -144,9 +147,20 @@ struct FwdItem {
   int bh;            // batch * Hq + query head
   int q0;            // first query row
   int kv_plane;      // batch * Hkv + key/value head
-  int n_tiles;       // K/V tiles the rows of this tile see
-  int first_masked;  // first of them that needs the causal or ragged-edge mask
+  int n_tiles;       // K/V tiles the rows of this tile see (those of the block pattern)
+  int j_begin;       // first key tile of the span
+  int lo_masked;     // key tiles below this need the window's lower-edge mask
+  int first_masked;  // key tiles from this on need the causal or ragged-edge mask
+  const uint8_t* pattern;  // this query tile's row of the block pattern, or null
 };
+
+// Key tiles of an item in order: j_begin, j_begin + 1, ... skipping those the block pattern
+// leaves out.  Every role walks the same sequence.
+__device__ __forceinline__ int next_kv_tile(const FwdItem& it, int j) {
+  if (it.pattern)
+    while (!it.pattern[j]) ++j;
+  return j;
+}
 
 // Work item `id` in launch order.  The (batch, query head) pairs are cut into groups of
 // head_group consecutive ones (the query heads of one key/value head are consecutive, and
@@ -167,7 +181,17 @@ __device__ __forceinline__ FwdItem decode_item(int id, const FwdParams& p) {
   const int h = it.bh % p.Hq;
   const int b = it.bh / p.Hq;
   it.kv_plane = b * p.Hkv + h / p.group;
-  kv_tile_range(qt, kBlockM, kBlockN, p.N_q, p.N_kv, p.causal, it.n_tiles, it.first_masked);
+  int j_end;
+  kv_tile_span(qt, kBlockM, kBlockN, p.N_q, p.N_kv, p.causal, p.window, it.j_begin, j_end,
+               it.lo_masked, it.first_masked);
+  it.pattern = nullptr;
+  it.n_tiles = j_end - it.j_begin;
+  if (p.block_mask) {
+    it.pattern = p.block_mask + static_cast<size_t>(qt) * p.n_kvtiles;
+    int n = 0;
+    for (int j = it.j_begin; j < j_end; ++j) n += it.pattern[j] ? 1 : 0;
+    it.n_tiles = n;
+  }
   return it;
 }
 
@@ -370,7 +394,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         next_id = -1;
         const FwdItem it = decode_item(id, p);
         if (it.n_tiles == 0) request_next();
-        for (int j = 0; j < it.n_tiles; ++j) {
+        for (int j = 0, kt = it.j_begin; j < it.n_tiles; ++j, ++kt) {
+          kt = next_kv_tile(it, kt);
           const int s = T % KS;
           if (T >= KS && !wait_bounded(BAR_KE(s), ((T / KS) - 1) & 1, abort_flag, p.status)) {
             ok = false;
@@ -380,7 +405,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int sub = 0; sub < D / 64; ++sub)
             tma_load_3d(sK + s * L::kKVBytes + sub * kSubTile, &tm_k, BAR_K(s), sub * 64,
-                        j * kBlockN, it.kv_plane);
+                        kt * kBlockN, it.kv_plane);
           ++T;
           if (j == 0) {
             if (kq >= 1 && !wait_bounded(FBAR(kBarQEmpty), (kq - 1) & 1, abort_flag, p.status)) {
@@ -425,7 +450,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!take_item(k, id)) break;
         if (id < 0) break;
         const FwdItem it = decode_item(id, p);
-        for (int j = 0; j < it.n_tiles; ++j) {
+        for (int j = 0, kt = it.j_begin; j < it.n_tiles; ++j, ++kt) {
+          kt = next_kv_tile(it, kt);
           const int s = T % VS;
           if (T >= VS && !wait_bounded(BAR_VE(s), ((T / VS) - 1) & 1, abort_flag, p.status)) {
             ok = false;
@@ -435,7 +461,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int sub = 0; sub < D / 64; ++sub)
             tma_load_3d(sV + s * L::kKVBytes + sub * kSubTile, &tm_v, BAR_V(s), sub * 64,
-                        j * kBlockN, it.kv_plane);
+                        kt * kBlockN, it.kv_plane);
           ++T;
         }
       }
@@ -640,8 +666,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const int T0 = T;
       const int T_last = T0 + n - 1;
-      for (int t = T0 + (((T0 & 1) != wg) ? 1 : 0); t <= T_last; t += 2) {
-        const int j = t - T0;  // K/V tile of the item
+      for (int i = 0, j = it.j_begin; i < n; ++i, ++j) {
+        j = next_kv_tile(it, j);  // key tile of the item's i-th tile
+        const int t = T0 + i;
+        if ((t & 1) != wg) continue;
         const int u = t >> 1;  // use index of this warpgroup's S and P buffers
         if (tracer) FWD_TRACE(t, 0);
         if (!__all_sync(0xffffffffu, s_ready) &&
@@ -674,6 +702,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             if (c > rel) x[c] = -INFINITY;
         }
+        if (j < it.lo_masked) {
+          // first visible key of this row under the sliding window
+          const int rel = row + off - p.window - j * kBlockN;
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            if (c < rel) x[c] = -INFINITY;
+        }
         // Row maximum of the tile: three-input max, eight independent chains.
         float mx[8];
 #pragma unroll
@@ -695,7 +730,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           m_read = mrow[r];
         }
-        const float m_prev = (j > 0) ? m_read : -INFINITY;
+        const float m_prev = (i > 0) ? m_read : -INFINITY;
         // The maximum moves only when it rises by more than 2^8 (also for the first finite one).
         float m_j = m_prev;
         float alpha = 1.0f;  // rescale of the accumulator O for this tile
@@ -742,7 +777,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st32(row_tmem + p_col + 32, pk[1]);
         // Both cases below need P V_{t-1} finished: P V_t waits for this tile's P and P V_{t+1}
         // comes after it, so nothing else touches the accumulator meanwhile.
-        const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
+        const bool rescale = i > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
         if (rescale || ep_pending) {
           if (!warp_wait(FBAR(kBarO + (wg ^ 1)), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
             ok = false;
@@ -868,7 +903,10 @@ static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
   p.N_kv = a.N_kv;
   p.n_qtiles = (a.N_q + kBlockM - 1) / kBlockM;
   p.group = a.Hq / a.Hkv;
-  p.causal = a.causal;
+  p.causal = (a.causal || a.window >= 0) ? 1 : 0;
+  p.window = a.window;
+  p.n_kvtiles = (a.N_kv + kBlockN - 1) / kBlockN;
+  p.block_mask = a.block_mask;
   p.BH = static_cast<int>(bhq);
   {
     // Query heads whose K/V planes fill about half of L2, a multiple of the heads sharing one

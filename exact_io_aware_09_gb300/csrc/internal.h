@@ -48,6 +48,38 @@ __host__ __device__ inline void kv_tile_range(int qt, int bm, int bn, int n_q, i
   first_masked = static_cast<int>(fm);
 }
 
+// Key-tile span of query tile qt (tiles of bm rows and bn keys) under the causal bound and an
+// optional sliding window of `window` keys behind the diagonal (window < 0: none; a window
+// implies the causal bound): the tiles [j_begin, j_end) hold every visible key; tiles below
+// lo_masked need the window's lower-edge mask and tiles from hi_masked on the upper
+// (causal or ragged-edge) mask.  An empty span has j_begin == j_end.
+__host__ __device__ inline void kv_tile_span(int qt, int bm, int bn, int n_q, int n_kv,
+                                             int causal, int window, int& j_begin, int& j_end,
+                                             int& lo_masked, int& hi_masked) {
+  int n = 0, fm = 0;
+  kv_tile_range(qt, bm, bn, n_q, n_kv, (causal || window >= 0) ? 1 : 0, n, fm);
+  j_begin = 0;
+  j_end = n;
+  lo_masked = 0;
+  hi_masked = fm;
+  if (window < 0 || n == 0) return;
+  const long long off = static_cast<long long>(n_kv) - n_q;
+  const long long r_first = static_cast<long long>(qt) * bm;
+  long long r_last = static_cast<long long>(qt + 1) * bm;
+  if (r_last > n_q) r_last = n_q;
+  r_last -= 1;
+  const long long lo_first = r_first + off - window;  // lowest key the first row sees
+  const long long lo_last = r_last + off - window;    // lowest key the last row sees
+  long long jb = lo_first > 0 ? lo_first / bn : 0;
+  long long lm = lo_last > 0 ? (lo_last + bn - 1) / bn : 0;  // tiles below see a cut
+  if (jb > n) jb = n;
+  if (lm < jb) lm = jb;
+  if (lm > n) lm = n;
+  j_begin = static_cast<int>(jb);
+  lo_masked = static_cast<int>(lm);
+  if (hi_masked < j_begin) hi_masked = j_begin;
+}
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -57,6 +89,8 @@ struct FwdArgs {
   int B, Hq, Hkv, N_q, N_kv, d, causal;
   float scale;
   bool bf16;
+  int window;                 // sliding window (keys behind the diagonal); -1 = none
+  const uint8_t* block_mask;  // [ceil(N_q/128)][ceil(N_kv/128)] tiles to compute; null = all
 };
 
 struct DecodeArgs {

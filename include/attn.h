@@ -90,6 +90,44 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              attn_dtype_t dtype);
 
 /*
+ * attn_fwd_window -- prefill attention with a sliding window, the mask that changes the
+ * operator ("FlashAttention Explained", FlexAttention section, sliding_causal: key kv is visible
+ * to query q iff q >= kv and q - kv <= W; "FlashAttention, annotated", section on causal masks
+ * and windows: key tiles outside the window are skipped, not masked).
+ *
+ * Arguments as attn_fwd, with `causal` replaced by
+ *   window   W >= 0: key j is visible to query row i iff 0 <= (i + N_kv - N_q) - j <= W
+ *            (bottom-right aligned as attn_fwd's causal mask, which W >= N_kv reproduces).
+ * Only the key tiles a query tile can see are loaded; the tiles cut by the window's lower edge
+ * or the diagonal are masked element by element.  A row with no visible key gets O = 0,
+ * L = -inf.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG (W < 0) or another attn_status_t.
+ */
+int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int Hq, int Hkv, int N_q, int N_kv, int d, int window, float scale,
+                    attn_stream_t stream, attn_dtype_t dtype);
+
+/*
+ * attn_fwd_block_sparse -- prefill attention restricted to a pattern of (query tile, key
+ * tile) blocks ("FlashAttention, annotated", section 3.3, block-sparse FlashAttention: a fixed
+ * pattern of tiles to compute and skip; the BlockMask of "FlashAttention Explained", one
+ * pattern shared by every batch and head).
+ *
+ * Arguments as attn_fwd, plus
+ *   block_mask  device pointer, uint8 [ceil(N_q / 128)][ceil(N_kv / 128)], row-major: nonzero
+ *               = compute query tile r (rows 128 r .. 128 r + 127) against key tile c (keys
+ *               128 c .. 128 c + 127).  Read-only; owned by the caller; read while the call
+ *               runs on `stream`.
+ * Keys outside listed blocks are invisible; inside a listed block the causal rule (if
+ * `causal`) still applies.  Unlisted blocks are neither loaded nor computed.  A row with no
+ * visible key gets O = 0, L = -inf.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null pattern) or
+ * another attn_status_t.
+ */
+int attn_fwd_block_sparse(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int Hq, int Hkv, int N_q, int N_kv, int d, int causal,
+                          const uint8_t *block_mask, float scale, attn_stream_t stream,
+                          attn_dtype_t dtype);
+
+/*
  * attn_decode_workspace_bytes -- device workspace attn_decode_splitkv needs.
  *
  * The split-KV decode writes one partial state (m, l, o[d]) per (sequence, query head,
@@ -190,6 +228,16 @@ const char *attn_status_string(int status);
  */
 int attn_fwd_kv_tiles(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
                       int *n_tiles, int *first_masked);
+
+/*
+ * attn_fwd_kv_span -- host-side copy of the key-tile span the prefill kernel walks for one
+ * query tile under a sliding window (window >= 0, which implies the causal bound) or none
+ * (window == -1): tiles *j_begin .. *j_end - 1 are loaded; tiles below *lo_masked need the
+ * window's lower-edge mask, tiles from *hi_masked on the diagonal or ragged-end mask.
+ * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_kv_span(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
+                     int window, int *j_begin, int *j_end, int *lo_masked, int *hi_masked);
 
 /*
  * attn_selftest_timeout -- launch one tiny kernel that waits on a barrier nothing ever

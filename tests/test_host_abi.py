@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -155,3 +156,33 @@ def test_bad_arguments_are_refused_before_launch(attn):
         assert dec() == -7
     assert L.attn_selftest_timeout(0, nul) == -1
     assert L.attn_selftest_timeout(2_000_000, nul) == -1
+
+
+@pytest.mark.parametrize("causal,window", [(True, -1), (False, -1), (True, 0), (True, 1),
+                                           (True, 127), (True, 128), (True, 300), (False, 1000)])
+def test_kv_span_covers_exactly_the_visible_keys(attn, causal, window):
+    """The key-tile span of each query tile holds every visible key and no tile without one;
+    the unmasked middle tiles are fully visible to every row."""
+    bm = bn = 128
+    for N_q, N_kv in [(1, 1), (300, 300), (200, 333), (333, 200), (129, 1000), (1000, 129)]:
+        off = N_kv - N_q
+        n_kvt = -(-N_kv // bn)
+        for qt in range(-(-N_q // bm)):
+            jb, je, lo, hi = attn.attn_fwd_kv_span(qt, bm, bn, N_q, N_kv, causal, window)
+            rows = np.arange(qt * bm, min(N_q, qt * bm + bm))
+            keys = np.arange(N_kv)
+            vis = np.ones((len(rows), N_kv), dtype=bool)
+            if causal or window >= 0:
+                vis &= keys[None, :] <= rows[:, None] + off
+            if window >= 0:
+                vis &= rows[:, None] + off - keys[None, :] <= window
+            for j in range(n_kvt):
+                tile = vis[:, j * bn:(j + 1) * bn]
+                if tile.any():
+                    assert jb <= j < je, (N_q, N_kv, qt, j, jb, je)
+                elif not (causal or window >= 0):
+                    continue
+                else:
+                    assert not (jb <= j < je) or j == jb or j == je - 1, (qt, j, jb, je)
+                if max(jb, lo) <= j < hi:
+                    assert tile.shape[1] == bn and tile.all(), (N_q, N_kv, qt, j, lo, hi)
