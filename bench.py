@@ -356,6 +356,11 @@ def run_ours(args):
     variants = None
     if do_pre and not args.no_variants:
         variants = measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
+    if do_dec and not args.no_variants:
+        variants = variants or {}
+        variants["decode_paged"] = measure_paged(args, attn, syn, dcfg, dq, dk, dv, do, dl, ws,
+                                                 lengths, max_len, dec_bytes, stream, peaks,
+                                                 peak_src)
 
     cpu = None
     if rank == 0 and world == 1 and do_pre and not args.no_cpu_baseline:
@@ -472,6 +477,48 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
                          "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
                          "frac": round(tf / peaks["bf16_tflops"], 4)},
         }
+    return out
+
+
+def measure_paged(args, attn, syn, dcfg, dq, dk, dv, do, dl, ws, lengths, max_len, dec_bytes,
+                  stream, peaks, peak_src):
+    """The decode step over a paged cache: the same cache scattered into shuffled 16-token
+    pages (vLLM's default block size) and read through the block table.  GB/s of the same
+    algorithmic bytes as the packed decode; timed like the variants."""
+    import torch
+
+    out = {}
+    for page_size in (16, 128):
+        table, n_pages, pg, sl = syn.paged_layout(lengths, page_size, seed=page_size)
+        kp = syn.scatter_to_pages(dk, n_pages, page_size, pg, sl)
+        vp = syn.scatter_to_pages(dv, n_pages, page_size, pg, sl)
+        tbl = torch.from_numpy(table).to(dq.device)
+        seq = torch.from_numpy(lengths.astype(np.int32)).to(dq.device)
+        fn = lambda: attn.attn_decode_paged(dq, kp, vp, tbl, seq, max_len, o=do, lse=dl,
+                                            split_size=dcfg.split, scale=dcfg.scale, workspace=ws,
+                                            stream=stream)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st = attn.attn_poll_status()
+        if st != 0:
+            raise SystemExit(f"device status after paged decode: {attn.attn_status_string(st)}")
+        ms = e0.elapsed_time(e1) / args.steps
+        gbs = dec_bytes / (ms / 1e3) / 1e9
+        out[f"page_{page_size}"] = {
+            "workload": f"the decode workload in shuffled {page_size}-token pages ({n_pages} pages)",
+            "ms_per_launch": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "peak_source": f"{peak_src} HBM copy",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4)},
+        }
+        del kp, vp
     return out
 
 

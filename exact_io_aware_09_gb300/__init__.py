@@ -47,6 +47,9 @@ lib.attn_decode_splitkv.restype = _I
 lib.attn_decode_splitkv_static.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I,
                                            _F, _I, _P]
 lib.attn_decode_splitkv_static.restype = _I
+lib.attn_decode_paged.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _I, _I, _F,
+                                  _I, _P, _SZ, _P]
+lib.attn_decode_paged.restype = _I
 lib.attn_decode_static_scratch_bytes.argtypes = []
 lib.attn_decode_static_scratch_bytes.restype = _SZ
 lib.attn_poll_status.argtypes = [_P]
@@ -194,6 +197,43 @@ def attn_fwd_kv_span(q_tile: int, block_m: int, block_n: int, N_q: int, N_kv: in
     _check(lib.attn_fwd_kv_span(q_tile, block_m, block_n, N_q, N_kv, int(bool(causal)),
                                 int(window), *[ctypes.byref(x) for x in out]), "attn_fwd_kv_span")
     return tuple(x.value for x in out)
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, max_seqlen_k: int, o=None,
+                      lse=None, split_size: int = 512, scale: float | None = None, workspace=None,
+                      stream=None):
+    """One split-KV decode step over a paged cache.
+
+    q [B,Hq,d]; k_pages/v_pages [num_pages, page_size, Hkv, d]; block_table int32 CUDA
+    [B, max_pages_per_seq]; seqlens_k int32 CUDA [B].  Returns (o [B,Hq,d], lse [B,Hq] fp32).
+    """
+    torch = _torch()
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    if v_pages.shape != k_pages.shape or k_pages.dtype != q.dtype or v_pages.dtype != q.dtype:
+        raise AttnError(-1, "attn_decode_paged: page pools disagree with q")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise AttnError(-1, "attn_decode_paged: block_table must be int32 [B, max_pages]")
+    if seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,):
+        raise AttnError(-1, "attn_decode_paged: seqlens_k must be int32 [B]")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    st = lib.attn_decode_paged(_dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"),
+                               _dev_ptr(v_pages, "v_pages"), _dev_ptr(block_table, "block_table"),
+                               _dev_ptr(seqlens_k, "seqlens_k"), num_pages, page_size,
+                               block_table.shape[1], int(max_seqlen_k), _dev_ptr(o, "o"),
+                               _dev_ptr(lse, "lse"), B, Hq, Hkv, d, int(split_size), float(scale),
+                               _dtype_code(q), _dev_ptr(workspace, "workspace"),
+                               workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_decode_paged")
+    return o, lse
 
 
 def attn_decode_workspace_bytes(B: int, Hq: int, max_seqlen_k: int, split_size: int, d: int) -> int:

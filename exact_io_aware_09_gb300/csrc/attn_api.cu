@@ -188,6 +188,46 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   return launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* block_table, const int32_t* seqlens_k, int num_pages,
+                      int page_size, int max_pages_per_seq, int max_seqlen_k, void* o, float* lse,
+                      int B, int Hq, int Hkv, int d, int split_size, float scale,
+                      attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                      attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_pages < 0 || max_pages_per_seq < 0 ||
+      max_seqlen_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (page_size < 16 || page_size > (1 << 16) || (page_size & (page_size - 1)) != 0)
+    return ATTN_ERR_UNSUPPORTED;
+  if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_pages_per_seq) * page_size < max_seqlen_k)
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  if (!q || !o || !lse || !block_table || !seqlens_k) return ATTN_ERR_INVALID_ARG;
+  if (max_seqlen_k > 0 && (num_pages == 0 || !k_pages || !v_pages)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  DecodeArgs a{q, k_pages, v_pages, nullptr, num_pages * page_size, max_seqlen_k, o, lse, B,
+               Hq, Hkv, d, split_size, scale, dtype == ATTN_BF16, workspace};
+  a.block_table = block_table;
+  a.seqlens = seqlens_k;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
+  return launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_decode_splitkv_static(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* cu_seqlens_k, int kv_capacity, int max_seqlen_k,
                                void* o, float* lse, int B, int Hq, int Hkv, int d, int split_size,

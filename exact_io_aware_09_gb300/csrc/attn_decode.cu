@@ -16,6 +16,12 @@
 // to 16 rows) straight from the swizzled stage buffers.  The four warps' states are merged in
 // shared memory and the chunk's normalised (m, l, o) is written to the workspace.
 // Kernel 2 (merge): one block per (sequence, query head) merges that row's chunk states.
+//
+// Paged cache ("FlashAttention Explained", section "Decoding, Paged and Split-KV Variants": the
+// cache in fixed-size non-contiguous blocks addressed through a block table, read by a split-KV
+// kernel): the same kernels with the producer reading each stage through the block table -- one
+// TMA box per stage when a page holds a whole 64-token stage, one box per page otherwise -- and
+// the sequence length taken from seqlens.
 #include <mutex>
 
 #include "internal.h"
@@ -31,7 +37,10 @@ constexpr int kMaxGroup = 16;    // query heads per key/value head (rows of the 
 
 struct DecParams {
   const uint16_t* q;   // [B, Hq, D]
-  const int32_t* cu;   // [B + 1]
+  const int32_t* cu;   // [B + 1] (packed cache)
+  const int32_t* block_table;  // [B, max_pages] (paged cache) or null
+  const int32_t* seqlens;      // [B] (paged cache)
+  int page_size, page_log2, max_pages, num_pages;
   float* ws_o;         // [B * Hq * max_splits, D]  normalised partial outputs
   float* ws_ml;        // [B * Hq * max_splits, 2]  (m in log2 units, l)
   int* status;
@@ -49,7 +58,10 @@ struct DecLayout {
   static_assert(kRed <= kRing, "merge scratch must fit in the ring");
   static constexpr uint32_t kBar = kRing;                        // full[S], empty[S]
   static constexpr uint32_t kMisc = kBar + 2 * kDecStages * 8;   // abort flag
-  static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+  // paged cache: first cache row of every page of the split (-1: not loaded)
+  static constexpr uint32_t kPages = kMisc + 16;
+  static constexpr int kMaxSplitPages = 8192 / 16;
+  static constexpr uint32_t kBytes = kPages + kMaxSplitPages * 4 + 1024;
 };
 
 __device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -63,6 +75,20 @@ __device__ __forceinline__ bool lengths_ok(const DecParams& p, int t_start, int 
   return t_start >= 0 && len >= 0 && len <= p.max_seqlen && t_stop <= p.capacity;
 }
 
+// Sequence b's tokens: rows [t_start, t_stop) of the packed cache, or logical positions
+// [0, seqlens[b]) of a paged one.  False for lengths the caller's bounds do not allow.
+__device__ __forceinline__ bool seq_bounds(const DecParams& p, int b, int& t_start, int& t_stop) {
+  if (p.block_table) {
+    t_start = 0;
+    t_stop = p.seqlens[b];
+    return t_stop >= 0 && t_stop <= p.max_seqlen &&
+           ((t_stop + p.page_size - 1) >> p.page_log2) <= p.max_pages;
+  }
+  t_start = p.cu[b];
+  t_stop = p.cu[b + 1];
+  return lengths_ok(p, t_start, t_stop);
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -71,9 +97,8 @@ __global__ void __launch_bounds__(kDecThreads)
   const int split = blockIdx.x;
   const int hk = blockIdx.y;
   const int b = blockIdx.z;
-  const int t_start = p.cu[b];
-  const int t_stop = p.cu[b + 1];
-  if (!lengths_ok(p, t_start, t_stop)) {
+  int t_start, t_stop;
+  if (!seq_bounds(p, b, t_start, t_stop)) {
     if (split == 0 && hk == 0 && threadIdx.x == 0) latch_status(p.status, kStatusBadLengths);
     return;
   }
@@ -107,6 +132,21 @@ __global__ void __launch_bounds__(kDecThreads)
 
   if (warp == kDecWarps) {
     // ------------------------------------------------------------------ TMA producer
+    int* page_row = reinterpret_cast<int*>(gbase + L::kPages);
+    if (p.block_table) {
+      // The split's block-table entries, read once by the whole warp: the first cache row of
+      // each page that holds tokens of the split, or -1 for an entry outside the pool (reported).
+      const int32_t* tbl = p.block_table + static_cast<size_t>(b) * p.max_pages;
+      const int first = t0 >> p.page_log2;
+      const int n_pg = ((t0 + n_tok - 1) >> p.page_log2) - first + 1;
+      for (int i = lane; i < n_pg; i += 32) {
+        const int pg = tbl[first + i];
+        const bool good = pg >= 0 && pg < p.num_pages;
+        if (!good) latch_status(p.status, kStatusBadLengths);
+        page_row[i] = good ? pg * p.page_size : -1;
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       int issued = 0;
       for (int st = 0; st < n_stages; ++st) {
@@ -116,11 +156,49 @@ __global__ void __launch_bounds__(kDecThreads)
           break;
         const uint32_t kbuf = base + s * L::kStage;
         const uint32_t vbuf = kbuf + L::kTensor;
-        mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
+        const int tl = t0 + st * kDecTok;  // first token of the stage
+        if (!p.block_table) {
+          mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
 #pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          tma_load_3d(kbuf + hh * L::kHalf, &tm_k, FULL(s), hh * 64, hk, t0 + st * kDecTok);
-          tma_load_3d(vbuf + hh * L::kHalf, &tm_v, FULL(s), hh * 64, hk, t0 + st * kDecTok);
+          for (int hh = 0; hh < D / 64; ++hh) {
+            tma_load_3d(kbuf + hh * L::kHalf, &tm_k, FULL(s), hh * 64, hk, tl);
+            tma_load_3d(vbuf + hh * L::kHalf, &tm_v, FULL(s), hh * 64, hk, tl);
+          }
+        } else {
+          // Pages of this stage that hold tokens of the sequence: one when a page spans the
+          // whole stage (its rows tl .. tl + 63 lie in one page), else 64 / page_size pages
+          // loaded to consecutive row blocks of the stage.  Rows past the sequence end are
+          // masked by the compute warps.  A block-table entry outside the page pool is
+          // reported and its load skipped.
+          const int rows = min(p.page_size, kDecTok);
+          const int n_pg = kDecTok / rows;
+          const int first = t0 >> p.page_log2;
+          uint32_t bytes = 0;
+          int phys[kDecTok / 16];
+#pragma unroll
+          for (int i = 0; i < kDecTok / 16; ++i) {
+            phys[i] = -1;
+            const int t = tl + i * rows;
+            if (i < n_pg && t < t_stop) {
+              const int r0 = page_row[(t >> p.page_log2) - first];
+              if (r0 >= 0) {
+                phys[i] = r0 + (t & (p.page_size - 1));
+                bytes += 2u * (D / 64) * rows * 128u;
+              }
+            }
+          }
+          mbar_arrive_expect_tx(FULL(s), bytes);
+#pragma unroll
+          for (int i = 0; i < kDecTok / 16; ++i) {
+            if (phys[i] < 0) continue;
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh) {
+              tma_load_3d(kbuf + hh * L::kHalf + i * rows * 128, &tm_k, FULL(s), hh * 64, hk,
+                          phys[i]);
+              tma_load_3d(vbuf + hh * L::kHalf + i * rows * 128, &tm_v, FULL(s), hh * 64, hk,
+                          phys[i]);
+            }
+          }
         }
         issued = st + 1;
       }
@@ -317,9 +395,8 @@ __global__ void __launch_bounds__(D)
   const int hq = blockIdx.x;
   const int b = blockIdx.y;
   const int col = threadIdx.x;
-  const int t_start = p.cu[b];
-  const int t_stop = p.cu[b + 1];
-  if (!lengths_ok(p, t_start, t_stop)) return;
+  int t_start, t_stop;
+  if (!seq_bounds(p, b, t_start, t_stop)) return;
   const int n_splits = (t_stop - t_start + p.split - 1) / p.split;
   const size_t row = static_cast<size_t>(b) * p.Hq + hq;
   if (n_splits == 0) {
@@ -357,13 +434,25 @@ static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
   const bool any_keys = a.kv_capacity > 0 && max_splits > 0;
   CUtensorMap tk, tv;
   const uint64_t row = static_cast<uint64_t>(D) * 2;
+  const bool paged = a.block_table != nullptr;
+  // the token axis: the packed cache, or every page of the pool end to end
+  const uint64_t tokens = paged ? static_cast<uint64_t>(a.num_pages) * a.page_size
+                                : static_cast<uint64_t>(a.kv_capacity);
+  const uint32_t box_rows = paged ? static_cast<uint32_t>(min(a.page_size, kDecTok)) : kDecTok;
   if (any_keys &&
-      (!make_tmap_3d(&tk, a.k_cache, BF16, D, a.Hkv, a.kv_capacity, row, row * a.Hkv, 64, 1, kDecTok) ||
-       !make_tmap_3d(&tv, a.v_cache, BF16, D, a.Hkv, a.kv_capacity, row, row * a.Hkv, 64, 1, kDecTok)))
+      (!make_tmap_3d(&tk, a.k_cache, BF16, D, a.Hkv, tokens, row, row * a.Hkv, 64, 1, box_rows) ||
+       !make_tmap_3d(&tv, a.v_cache, BF16, D, a.Hkv, tokens, row, row * a.Hkv, 64, 1, box_rows)))
     return -5;
   DecParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.cu = a.cu_seqlens;
+  p.block_table = a.block_table;
+  p.seqlens = a.seqlens;
+  p.page_size = a.page_size;
+  p.page_log2 = 0;
+  while (paged && (1 << p.page_log2) < a.page_size) ++p.page_log2;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   const size_t parts = static_cast<size_t>(a.B) * a.Hq * (max_splits > 0 ? max_splits : 1);
   p.ws_o = static_cast<float*>(a.workspace);
   p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(a.workspace) +

@@ -105,6 +105,12 @@ struct DecodeArgs {
   float scale;
   bool bf16;
   void* workspace;
+  // paged cache (block_table != null): k_cache/v_cache are [num_pages, page_size, Hkv, d],
+  // sequence b's token t is row t % page_size of page block_table[b * max_pages + t / page_size],
+  // and seqlens[b] replaces cu_seqlens
+  const int32_t* block_table = nullptr;
+  const int32_t* seqlens = nullptr;
+  int page_size = 0, max_pages = 0, num_pages = 0;
 };
 
 // Launchers (return an attn_status_t value).

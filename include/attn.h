@@ -201,6 +201,35 @@ int attn_decode_splitkv_static(const void *q, const void *k_cache, const void *v
                                int split_size, float scale, attn_dtype_t dtype,
                                attn_stream_t stream);
 
+/*
+ * attn_decode_paged -- the split-KV decode step over a paged KV cache ("FlashAttention
+ * Explained", section "Decoding, Paged and Split-KV Variants": PagedAttention stores the cache
+ * in fixed-size non-contiguous blocks addressed through a block table; production engines run
+ * split-KV decoding over it).
+ *
+ *   q             [B, Hq, d] device, contiguous, the new token of every sequence
+ *   k_pages,
+ *   v_pages       [num_pages, page_size, Hkv, d] device, contiguous: the page pool
+ *   block_table   [B, max_pages_per_seq] int32 device: sequence b's token t is row
+ *                 t % page_size of page block_table[b * max_pages_per_seq + t / page_size];
+ *                 entries past the sequence's last page are not read
+ *   seqlens_k     [B] int32 device: cached tokens of each sequence (0 allowed: O = 0, L = -inf)
+ *   num_pages     pages in the pool; page_size a power of two from 16 to 65536
+ *   max_seqlen_k  upper bound of seqlens_k (<= max_pages_per_seq * page_size), sizes the grid
+ *   o, lse, B, Hq, Hkv, d, split_size, scale, dtype, workspace, workspace_bytes, stream
+ *                 as attn_decode_splitkv (the workspace size is attn_decode_workspace_bytes)
+ * The result equals attn_decode_splitkv on the gathered packed cache.  A length above
+ * max_seqlen_k or a block-table entry outside [0, num_pages) is reported as
+ * ATTN_ERR_BAD_LENGTHS by attn_poll_status (that sequence's output is then undefined).
+ * Returns ATTN_OK or a negative attn_status_t.
+ */
+int attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *block_table, const int32_t *seqlens_k, int num_pages,
+                      int page_size, int max_pages_per_seq, int max_seqlen_k, void *o, float *lse,
+                      int B, int Hq, int Hkv, int d, int split_size, float scale,
+                      attn_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                      attn_stream_t stream);
+
 /* attn_decode_static_scratch_bytes -- size of the scratch attn_decode_splitkv_static uses. */
 size_t attn_decode_static_scratch_bytes(void);
 

@@ -168,6 +168,31 @@ def attention(q, k, v, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale, threads: in
     return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
 
 
+def gather_pages(pages, block_table, seqlens, page_size):
+    """The packed [sum(L), Hkv, d] cache of a paged one: sequence b's token t is row
+    t % page_size of page block_table[b][t // page_size] ("FlashAttention Explained", section
+    "Decoding, Paged and Split-KV Variants": fixed-size non-contiguous blocks addressed through
+    a block table).  pages: [num_pages, page_size, Hkv, d]."""
+    pages = np.asarray(pages)
+    out = []
+    for b, L in enumerate(np.asarray(seqlens, dtype=np.int64)):
+        t = np.arange(int(L), dtype=np.int64)
+        out.append(pages[np.asarray(block_table)[b][t // page_size], t % page_size])
+    if not out:
+        return pages[:0, 0]
+    return np.ascontiguousarray(np.concatenate(out, axis=0))
+
+
+def decode_rows_paged(q, k_pages, v_pages, block_table, seqlens, page_size, dtype, B, Hq, Hkv,
+                      d, scale, rows=None, threads: int = 0):
+    """Decode attention over a paged cache: the packed definition of the gathered cache."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    kc = gather_pages(k_pages, block_table, seqlens, page_size)
+    vc = gather_pages(v_pages, block_table, seqlens, page_size)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    return decode_rows(q, kc, vc, cu, dtype, B, Hq, Hkv, d, scale, rows, threads)
+
+
 def decode_rows(q, k_cache, v_cache, cu_seqlens, dtype, B, Hq, Hkv, d, scale, rows=None,
                 threads: int = 0):
     """Decode attention (one query token per sequence, packed [T, Hkv, d] cache).

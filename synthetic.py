@@ -199,3 +199,51 @@ CONFIG4 = PrefillConfig("gqa_causal_b1_hq64_hkv8_n8192_d128_bf16", 1, 64, 8, 819
 CONFIG5 = DecodeConfig("splitkv_decode_b64_hq64_hkv8_d128_bf16", 64, 64, 8, 128, BF16, 5001)
 
 PREFILL_CONFIGS = [CONFIG1, CONFIG2, CONFIG3A, CONFIG3B, CONFIG3SA, CONFIG3SB, CONFIG4]
+
+
+# ----------------------------------------------------------------------------------------
+# paged KV cache layout (input generation only: where each token of a packed cache goes)
+# ----------------------------------------------------------------------------------------
+def paged_layout(lengths, page_size: int, seed: int, spare_pages: int = 3):
+    """A shuffled page pool for sequences of the given lengths.
+
+    Returns (block_table int32 [B, max_pages] padded with -1, num_pages, page_of_token,
+    slot_of_token): packed token cu[b] + t of sequence b goes to row slot_of_token of page
+    page_of_token.  spare_pages unused pages are added to the pool.
+    """
+    lengths = np.asarray(lengths, dtype=np.int64)
+    n_pages = (lengths + page_size - 1) // page_size
+    num_pages = int(n_pages.sum()) + spare_pages
+    perm = np.random.default_rng(seed).permutation(num_pages).astype(np.int32)
+    max_pages = max(1, int(n_pages.max()) if len(n_pages) else 1)
+    table = np.full((len(lengths), max_pages), -1, dtype=np.int32)
+    page_of_token, slot_of_token = [], []
+    used = 0
+    for b, L in enumerate(lengths):
+        table[b, :n_pages[b]] = perm[used:used + n_pages[b]]
+        used += int(n_pages[b])
+        t = np.arange(int(L), dtype=np.int64)
+        page_of_token.append(table[b][t // page_size].astype(np.int64))
+        slot_of_token.append(t % page_size)
+    cat = lambda xs: np.concatenate(xs) if xs else np.zeros(0, dtype=np.int64)
+    return table, num_pages, cat(page_of_token), cat(slot_of_token)
+
+
+def scatter_to_pages(cache, num_pages, page_size, page_of_token, slot_of_token, fill=None):
+    """[T, Hkv, d] packed cache (numpy or torch) -> [num_pages, page_size, Hkv, d] pool; rows no
+    token occupies hold `fill` (numpy: random bits of the given generator seed; torch: NaN)."""
+    if isinstance(cache, np.ndarray):
+        shape = (num_pages, page_size) + cache.shape[1:]
+        if fill is None:
+            pool = np.zeros(shape, dtype=cache.dtype)
+        else:
+            pool = np.random.default_rng(fill).integers(0, 65535, size=shape).astype(cache.dtype)
+        pool[page_of_token, slot_of_token] = cache
+        return pool
+    import torch
+
+    pool = torch.full((num_pages, page_size) + tuple(cache.shape[1:]), float("nan"),
+                      dtype=cache.dtype, device=cache.device)
+    pool[torch.from_numpy(page_of_token).to(cache.device),
+         torch.from_numpy(slot_of_token).to(cache.device)] = cache
+    return pool

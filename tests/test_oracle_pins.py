@@ -545,3 +545,40 @@ def test_block_mask_row_is_full_attention_over_listed_blocks(causal):
         of, lf = oracle.attention_rows(qs, ks, vs, BF16, 1, 1, 1, 1, len(keys), d, False, cfg.scale)
         np.testing.assert_allclose(o[i], of[0], rtol=0, atol=1e-14)
         assert abs(lse[i] - lf[0]) < 1e-13
+
+
+# ------------------------------------------------------------------------------------
+# paged KV cache: an addressing scheme over the same definition
+# ("FlashAttention Explained", section "Decoding, Paged and Split-KV Variants")
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("page_size", [1, 16, 64])
+def test_paged_decode_is_the_packed_definition(page_size):
+    lengths = [0, 1, 37, 130, 64]
+    Hq, Hkv, d = 8, 2, 16
+    cfg = syn.DecodeConfig("pg", len(lengths), Hq, Hkv, d, BF16, 123, lengths_override=tuple(lengths))
+    q, kc, vc = cfg.host_inputs()
+    cu = syn.cu_seqlens(lengths)
+    ref_o, ref_l = oracle.decode_rows(q, kc, vc, cu, BF16, cfg.B, Hq, Hkv, d, cfg.scale)
+    # scatter the packed cache into shuffled pages, leaving unused pages full of garbage
+    rng = np.random.default_rng(page_size)
+    n_pages = [-(-L // page_size) for L in lengths]
+    total = sum(n_pages) + 5
+    perm = rng.permutation(total)
+    kp = rng.integers(0, 65535, size=(total, page_size, Hkv, d)).astype(np.uint16)
+    vp = rng.integers(0, 65535, size=(total, page_size, Hkv, d)).astype(np.uint16)
+    table = np.full((len(lengths), max(n_pages)), -1, dtype=np.int32)
+    used = 0
+    for b, L in enumerate(lengths):
+        for pg in range(n_pages[b]):
+            phys = perm[used]
+            used += 1
+            table[b, pg] = phys
+            t = np.arange(pg * page_size, min(L, (pg + 1) * page_size))
+            kp[phys, t - pg * page_size] = kc[cu[b] + t]
+            vp[phys, t - pg * page_size] = vc[cu[b] + t]
+    o, lse = oracle.decode_rows_paged(q, kp, vp, table, lengths, page_size, BF16, cfg.B, Hq, Hkv, d,
+                                      cfg.scale)
+    np.testing.assert_array_equal(o, ref_o)
+    np.testing.assert_array_equal(lse, ref_l)
+    # the gather itself: every token of every sequence comes back in order
+    np.testing.assert_array_equal(oracle.gather_pages(kp, table, lengths, page_size), kc)
