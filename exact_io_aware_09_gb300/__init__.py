@@ -34,6 +34,11 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
 lib.attn_fwd.restype = _I
+lib.attn_bwd_workspace_bytes.argtypes = [_I, _I, _I]
+lib.attn_bwd_workspace_bytes.restype = _SZ
+lib.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
+                         _SZ, _P]
+lib.attn_bwd.restype = _I
 lib.attn_fwd_window.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
 lib.attn_fwd_window.restype = _I
 lib.attn_fwd_block_sparse.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P,
@@ -155,6 +160,38 @@ def _fwd_prep(q, k, v, o, lse, scale):
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     return B, Hq, Hkv, N_q, N_kv, d, o, lse, float(scale)
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the incoming gradient ``dout`` (shape of o).
+
+    q/o/dout [B,Hq,N_q,d], k/v [B,Hkv,N_kv,d] 16-bit CUDA tensors, lse [B,Hq,N_q] fp32 as
+    attn_fwd returns it.  Deterministic.
+    """
+    torch = _torch()
+    B, Hq, N_q, d = q.shape
+    _, Hkv, N_kv, _ = k.shape
+    for t, nm in ((o, "o"), (dout, "dout")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise AttnError(-1, f"attn_bwd: {nm} must match q")
+    if k.shape != v.shape or k.dtype != q.dtype or v.dtype != q.dtype or lse.dtype != torch.float32:
+        raise AttnError(-1, "attn_bwd: k/v/lse shapes or dtypes disagree")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.attn_bwd_workspace_bytes(B, Hq, N_q)), 1),
+                                device=q.device, dtype=torch.uint8)
+    st = lib.attn_bwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                      _dev_ptr(dout, "dout"), _dev_ptr(lse, "lse"), _dev_ptr(dq, "dq"),
+                      _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), B, Hq, Hkv, N_q, N_kv, d,
+                      int(bool(causal)), float(scale), _dtype_code(q),
+                      _dev_ptr(workspace, "workspace"), workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_window(q, k, v, window: int, o=None, lse=None, scale: float | None = None,

@@ -157,6 +157,43 @@ int attn_fwd_kv_span(int q_tile, int block_m, int block_n, int N_q, int N_kv, in
   return ATTN_OK;
 }
 
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N_q) { return bwd_workspace_bytes(B, Hq, N_q); }
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N_q,
+             int N_kv, int d, int causal, float scale, attn_dtype_t dtype, void* workspace,
+             size_t workspace_bytes, attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N_q < 0 || N_kv < 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || (N_q == 0 && N_kv == 0)) return ATTN_OK;
+  if ((N_q > 0 && (!q || !o || !dout || !lse || !dq)) || (N_kv > 0 && (!k || !v || !dk || !dv)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (N_q == 0 || N_kv == 0) {
+    // no (query, key) pair: every gradient is zero
+    if (N_q > 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Hq * N_q * d * 2, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    if (N_kv > 0 &&
+        (cudaMemsetAsync(dk, 0, static_cast<size_t>(B) * Hkv * N_kv * d * 2, st) != cudaSuccess ||
+         cudaMemsetAsync(dv, 0, static_cast<size_t>(B) * Hkv * N_kv * d * 2, st) != cudaSuccess))
+      return ATTN_ERR_LAUNCH;
+    return ATTN_OK;
+  }
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(B, Hq, N_q)) return ATTN_ERR_WORKSPACE;
+  BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale,
+            dtype == ATTN_BF16, workspace};
+  return launch_attn_bwd(a, st);
+}
+
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_size, int d) {
   return decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
 }

@@ -1,0 +1,666 @@
+// Backward pass of exact attention by recomputation, sm_103a.
+//
+// "FlashAttention Explained", section "Backward Pass: Recomputation Beats Storage": the forward
+// pass saves O and one log-sum-exp L per row; the backward pass recomputes the score and
+// probability tiles from Q, K and L (P = exp(S - L)) and forms
+//     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D) with D_i = rowsum(dO_i o O_i),
+//     dQ = scale dS K,  dK = scale dS^T Q.
+// The pages note that accumulating dQ across key tiles with atomic adds makes the result
+// nondeterministic.  Here every gradient is owned by exactly one thread block, so the result is
+// deterministic by construction:
+//   kernel 0  D and L log2(e) per query row (padded to whole 128-row tiles);
+//   kernel 1  one block per 128-key tile of one (batch, key/value head): loops over the query
+//             tiles of every query head that shares the key/value head and keeps dK and dV in
+//             tensor memory (four MMAs per tile pair: S^T, dP^T, dV += P^T dO, dK += dS^T Q);
+//   kernel 2  one block per 128-row query tile: loops over the key tiles and keeps dQ in
+//             tensor memory (three MMAs per tile pair: S, dP, dQ += dS K).
+// S and dP are recomputed in both kernels (seven MMAs per tile pair instead of five): the price
+// of owning every output without atomics.
+//
+// Roles inside a thread block (192 threads): warps 0-3 the elementwise step (thread = one row of
+// the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 4 the TMA producer,
+// warp 5 the tcgen05 issuer (and the tensor-memory allocation).  Both probabilities and dS go
+// back to tensor memory as 16-bit pairs, in place over the fp32 tiles they came from, and feed
+// the next MMAs as their A operand.  Every wait on a barrier is bounded.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kBT = 128;            // rows of a query tile and keys of a key tile
+constexpr int kBwdThreads = 192;
+constexpr int kEwThreads = 128;     // elementwise warpgroup
+constexpr int kBwdProducerWarp = 4, kBwdIssuerWarp = 5;
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzled sub-tile
+constexpr uint64_t kBwdDrainNs = 100000000ull;
+
+struct BwdParams {
+  const float* lse2;  // [B*Hq, nqp]  L * log2(e); +inf on padding rows
+  const float* dvec;  // [B*Hq, nqp]  D; 0 on padding rows
+  uint16_t* dq;       // [B, Hq, N_q, d]
+  uint16_t* dk;       // [B, Hkv, N_kv, d]
+  uint16_t* dv;
+  int* status;
+  int Hq, Hkv, G, N_q, N_kv, n_qtiles, n_kvtiles, nqp, causal;
+  float sl2;    // scale * log2(e)
+  float scale;
+};
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_f32(uint32_t h) {
+  if constexpr (BF16) {
+    return __uint_as_float(h << 16);
+  } else {
+    float f;
+    asm("{\n\t.reg .f16 t;\n\tmov.b16 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "h"(static_cast<uint16_t>(h)));
+    return f;
+  }
+}
+
+__device__ __forceinline__ bool ew_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                        int* status) {
+  const bool ok = wait_bounded(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One 128 x D tile row r of a tensor-memory accumulator -> 16-bit values of global row `dst`.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_acc_row(uint32_t row_tmem_col, uint16_t* dst, bool store) {
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t a[32];
+    tmem_ld32(row_tmem_col + c * 32, a);
+    tmem_wait_ld();
+    if (store) {
+      uint4* out = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        out[q4] = make_uint4(pack2<BF16>(__uint_as_float(a[8 * q4 + 0]), __uint_as_float(a[8 * q4 + 1])),
+                             pack2<BF16>(__uint_as_float(a[8 * q4 + 2]), __uint_as_float(a[8 * q4 + 3])),
+                             pack2<BF16>(__uint_as_float(a[8 * q4 + 4]), __uint_as_float(a[8 * q4 + 5])),
+                             pack2<BF16>(__uint_as_float(a[8 * q4 + 6]), __uint_as_float(a[8 * q4 + 7])));
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_zero_row(uint16_t* dst) {
+  uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) out[c] = make_uint4(0, 0, 0, 0);
+}
+
+// K-major A x K-major B^T, both 128 rows x D (the two 64-column halves of d are separate swizzled
+// sub-tiles): D[128 x 128] (+)= A B^T.
+template <int D>
+__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                              uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+    mma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// A [128 x 128] in tensor memory (16-bit pairs, 64 columns) times B [128 rows x D] in shared
+// memory read MN-major: D[128 x D] (+)= A B.
+__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                              uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBT / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 16 * 128, kSub, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------
+// kernel 0: D = rowsum(dO o O) and L log2(e), one warp per (padded) query row
+// ------------------------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
+                                    float* lse2, float* dvec, int N_q, int nqp, long long rows) {
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rows) return;
+  const long long bh = w / nqp;
+  const int i = static_cast<int>(w - bh * nqp);
+  float acc = 0.0f;
+  if (i < N_q) {
+    const size_t base = (static_cast<size_t>(bh) * N_q + i) * D;
+    const uint32_t* o2 = reinterpret_cast<const uint32_t*>(o + base);
+    const uint32_t* d2 = reinterpret_cast<const uint32_t*>(dout + base);
+#pragma unroll
+    for (int c = lane; c < D / 2; c += 32) {
+      const uint32_t a = o2[c], b = d2[c];
+      acc = fmaf(half_to_f32<BF16>(a & 0xffffu), half_to_f32<BF16>(b & 0xffffu), acc);
+      acc = fmaf(half_to_f32<BF16>(a >> 16), half_to_f32<BF16>(b >> 16), acc);
+    }
+  }
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (lane == 0) {
+    dvec[w] = (i < N_q) ? acc : 0.0f;
+    lse2[w] = (i < N_q) ? lse[bh * N_q + i] * 1.4426950408889634f : INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// kernel 1: dK, dV of one 128-key tile
+// ------------------------------------------------------------------------------------------
+template <int D, int QS>
+struct KvLayout {
+  static constexpr uint32_t kTile = kBT * D * 2;
+  static constexpr uint32_t kStage = 2 * kTile + 1024;  // Q, dO, then L log2(e) and D [128] each
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kTile;
+  static constexpr uint32_t kStages = 2 * kTile;
+  static constexpr uint32_t kBar = kStages + QS * kStage;
+  // kv_full, st_full[QS], st_empty[QS], sdp_full, pds_ready, mm_done, drain
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 4;
+  static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+  static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tile alignment");
+  static_assert(kBytes <= 232448, "shared memory per block");
+};
+
+template <int D, bool BF16, int QS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = KvLayout<D, QS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + L::kBar;
+  const uint32_t bar_kv = bars;
+#define ST_FULL(s) (bars + 8u * (1 + (s)))
+#define ST_EMPTY(s) (bars + 8u * (1 + QS + (s)))
+  const uint32_t bar_sdp = bars + 8u * (1 + 2 * QS);
+  const uint32_t bar_pds = bar_sdp + 8;
+  const uint32_t bar_mm = bar_sdp + 16;
+  const uint32_t bar_drain = bar_sdp + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // item: key tile kt of (batch, key/value head) bkv; small kt first (most query tiles)
+  const int bkv = blockIdx.x / p.n_kvtiles;
+  const int kt = static_cast<int>(blockIdx.x % p.n_kvtiles);
+  const int b = bkv / p.Hkv;
+  const int hk = bkv % p.Hkv;
+  const int off = p.N_kv - p.N_q;
+  int qt_lo = 0;
+  if (p.causal) {
+    const int first_row = kt * kBT - off;  // first query row that sees key kt * 128
+    qt_lo = first_row > 0 ? first_row / kBT : 0;
+  }
+  const int nq_per = p.n_qtiles - qt_lo;  // query tiles per query head
+  const int n = nq_per > 0 ? p.G * nq_per : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(ST_FULL(s), 1);
+      mbar_init(ST_EMPTY(s), 1);
+    }
+    mbar_init(bar_sdp, 1);
+    mbar_init(bar_pds, kEwThreads);
+    mbar_init(bar_mm, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kBwdIssuerWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+
+  if (warp == kBwdProducerWarp) {
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(bar_kv, 2 * L::kTile);
+#pragma unroll
+      for (int sub = 0; sub < D / 64; ++sub) {
+        tma_load_3d(base + L::kK + sub * kSub, &tm_k, bar_kv, sub * 64, kt * kBT, bkv);
+        tma_load_3d(base + L::kV + sub * kSub, &tm_v, bar_kv, sub * 64, kt * kBT, bkv);
+      }
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % QS;
+        if (i >= QS && !wait_bounded(ST_EMPTY(s), ((i / QS) - 1) & 1, abort_flag, p.status)) break;
+        const int g = i / nq_per;
+        const int qt = qt_lo + i % nq_per;
+        const int bhq = b * p.Hq + hk * p.G + g;
+        const uint32_t st = base + L::kStages + s * L::kStage;
+        mbar_arrive_expect_tx(ST_FULL(s), 2 * L::kTile + 1024);
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub) {
+          tma_load_3d(st + sub * kSub, &tm_q, ST_FULL(s), sub * 64, qt * kBT, bhq);
+          tma_load_3d(st + L::kTile + sub * kSub, &tm_do, ST_FULL(s), sub * 64, qt * kBT, bhq);
+        }
+        const size_t vec = static_cast<size_t>(bhq) * p.nqp + static_cast<size_t>(qt) * kBT;
+        bulk_load(st + 2 * L::kTile, p.lse2 + vec, kBT * 4, ST_FULL(s));
+        bulk_load(st + 2 * L::kTile + 512, p.dvec + vec, kBT * 4, ST_FULL(s));
+        issued = i + 1;
+      }
+      wait_bounded(bar_kv, 0, nullptr, p.status, kBwdDrainNs);
+      for (int i = (issued > QS ? issued - QS : 0); i < issued; ++i)
+        wait_bounded(ST_FULL(i % QS), (i / QS) & 1, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == kBwdIssuerWarp) {
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
+      constexpr uint32_t idesc_tr = make_idesc_f16(BF16, kBT, D, true);
+      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status);
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % QS;
+        const uint32_t st = base + L::kStages + s * L::kStage;
+        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) break;
+        // S^T and dP^T of the previous tile were read as A operands by its last MMAs
+        if (i > 0 && !wait_bounded(bar_mm, (i - 1) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + kColS, base + L::kK, st, idesc_rr);               // S^T = K Q^T
+        mma_rows_rows<D>(tmem + kColDP, base + L::kV, st + L::kTile, idesc_rr);   // dP^T = V dO^T
+        mma_commit(bar_sdp);
+        if (!wait_bounded(bar_pds, i & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        mma_tmem_rows(tmem + kColDV, tmem + kColS, st + L::kTile, idesc_tr, i > 0);  // dV += P^T dO
+        mma_tmem_rows(tmem + kColDK, tmem + kColDP, st, idesc_tr, i > 0);           // dK += dS^T Q
+        mma_commit(bar_mm);
+        mma_commit(ST_EMPTY(s));
+      }
+      mma_commit(bar_drain);
+      wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise (thread = key)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int kr = kt * kBT + r;  // this thread's key
+    const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.sl2, scale = p.scale;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % QS;
+      const int qt = qt_lo + i % nq_per;
+      const float* lv = reinterpret_cast<const float*>(gbase + L::kStages + s * L::kStage + 2 * L::kTile);
+      const float* dvv = lv + kBT;
+      if (!ew_wait(bar_sdp, i & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // keys above this bound are masked for query row q: key <= q + off
+      const int q_first_visible = kr - off;  // the smallest query row that sees this key
+#pragma unroll 1
+      for (int c4 = 0; c4 < kBT / 32; ++c4) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(row_tmem + kColS + c4 * 32, sv);
+        tmem_ld32(row_tmem + kColDP + c4 * 32, dpv);
+        tmem_wait_ld();
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = c4 * 32 + e;
+          const int qrow = qt * kBT + col;
+          const float4 l4 = *reinterpret_cast<const float4*>(lv + (col & ~3));
+          const float4 d4 = *reinterpret_cast<const float4*>(dvv + (col & ~3));
+          const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
+          const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
+          const bool va = !p.causal || qrow >= q_first_visible;
+          const bool vb = !p.causal || qrow + 1 >= q_first_visible;
+          const float pa = va ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -la)) : 0.0f;
+          const float pb = vb ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lb)) : 0.0f;
+          const float dsa = pa * (__uint_as_float(dpv[e]) - da) * scale;
+          const float dsb = pb * (__uint_as_float(dpv[e + 1]) - db) * scale;
+          pp[e >> 1] = pack2<BF16>(pa, pb);
+          dd[e >> 1] = pack2<BF16>(dsa, dsb);
+        }
+        // in place: these columns belong to chunks already read
+        tmem_st16(row_tmem + kColS + c4 * 16, pp);
+        tmem_st16(row_tmem + kColDP + c4 * 16, dd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_pds);
+    }
+    // epilogue: dV and dK rows of this key tile
+    if (ok && n > 0) ok = ew_wait(bar_mm, (n - 1) & 1, abort_flag, p.status);
+    if (ok) {
+      tc_fence_after();
+      const bool store = kr < p.N_kv;
+      const size_t grow = (static_cast<size_t>(bkv) * p.N_kv + (store ? kr : 0)) * D;
+      if (n > 0) {
+        store_acc_row<D, BF16>(row_tmem + kColDV, p.dv + grow, store);
+        store_acc_row<D, BF16>(row_tmem + kColDK, p.dk + grow, store);
+      } else if (store) {
+        store_zero_row<D>(p.dv + grow);
+        store_zero_row<D>(p.dk + grow);
+      }
+    }
+  }
+#undef ST_FULL
+#undef ST_EMPTY
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdIssuerWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// kernel 2: dQ of one 128-row query tile
+// ------------------------------------------------------------------------------------------
+template <int D, int KS>
+struct QLayout {
+  static constexpr uint32_t kTile = kBT * D * 2;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kDO = kTile;
+  static constexpr uint32_t kK = 2 * kTile;            // K ring, KS slots
+  static constexpr uint32_t kV = kK + KS * kTile;      // V ring, KS slots
+  static constexpr uint32_t kBar = kV + KS * kTile;
+  // q_full, k_full[KS], k_empty[KS], v_full[KS], v_empty[KS], sdp_full, s_free[2], ds_ready,
+  // dq_done, drain
+  static constexpr uint32_t kNumBars = 1 + 4 * KS + 6;
+  static constexpr uint32_t kMisc = kBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+  static_assert(kBytes <= 232448, "shared memory per block");
+};
+
+template <int D, bool BF16, int KS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = QLayout<D, KS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + L::kBar;
+  const uint32_t bar_q = bars;
+#define K_FULL(s) (bars + 8u * (1 + (s)))
+#define K_EMPTY(s) (bars + 8u * (1 + KS + (s)))
+#define V_FULL(s) (bars + 8u * (1 + 2 * KS + (s)))
+#define V_EMPTY(s) (bars + 8u * (1 + 3 * KS + (s)))
+  const uint32_t bar_sdp = bars + 8u * (1 + 4 * KS);
+#define S_FREE(b) (bar_sdp + 8u * (1 + (b)))
+  const uint32_t bar_ds = bar_sdp + 24;
+  const uint32_t bar_dq = bar_sdp + 32;
+  const uint32_t bar_drain = bar_sdp + 40;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // item: query tile qt of (batch, query head) bh; longest query tiles first
+  const int bh = blockIdx.x / p.n_qtiles;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
+  const int kv_plane = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.G;
+  int n, first_masked;
+  kv_tile_range(qt, kBT, kBT, p.N_q, p.N_kv, p.causal, n, first_masked);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(K_FULL(s), 1);
+      mbar_init(K_EMPTY(s), 1);
+      mbar_init(V_FULL(s), 1);
+      mbar_init(V_EMPTY(s), 1);
+    }
+    mbar_init(bar_sdp, 1);
+    mbar_init(S_FREE(0), kEwThreads);
+    mbar_init(S_FREE(1), kEwThreads);
+    mbar_init(bar_ds, kEwThreads);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kBwdIssuerWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // S double-buffered, one dP buffer (dS written over it), the dQ accumulator
+  constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
+
+  if (warp == kBwdProducerWarp) {
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+#pragma unroll
+      for (int sub = 0; sub < D / 64; ++sub) {
+        tma_load_3d(base + L::kQ + sub * kSub, &tm_q, bar_q, sub * 64, qt * kBT, bh);
+        tma_load_3d(base + L::kDO + sub * kSub, &tm_do, bar_q, sub * 64, qt * kBT, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int s = t % KS;
+        if (t >= KS && !wait_bounded(K_EMPTY(s), ((t / KS) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(K_FULL(s), L::kTile);
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub)
+          tma_load_3d(base + L::kK + s * L::kTile + sub * kSub, &tm_k, K_FULL(s), sub * 64, t * kBT,
+                      kv_plane);
+        if (t >= KS && !wait_bounded(V_EMPTY(s), ((t / KS) - 1) & 1, abort_flag, p.status)) {
+          issued = t + 1;  // K_t is in flight
+          break;
+        }
+        mbar_arrive_expect_tx(V_FULL(s), L::kTile);
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub)
+          tma_load_3d(base + L::kV + s * L::kTile + sub * kSub, &tm_v, V_FULL(s), sub * 64, t * kBT,
+                      kv_plane);
+        issued = t + 1;
+      }
+      wait_bounded(bar_q, 0, nullptr, p.status, kBwdDrainNs);
+      for (int t = (issued > KS ? issued - KS : 0); t < issued; ++t) {
+        wait_bounded(K_FULL(t % KS), (t / KS) & 1, nullptr, p.status, kBwdDrainNs);
+        wait_bounded(V_FULL(t % KS), (t / KS) & 1, nullptr, p.status, kBwdDrainNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kBwdIssuerWarp) {
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
+      constexpr uint32_t idesc_tr = make_idesc_f16(BF16, kBT, D, true);
+      // S_t = Q K_t^T into S buffer t % 2 once the elementwise step of tile t - 2 has read it
+      auto issue_s = [&](int t) -> bool {
+        if (t >= 2 && !wait_bounded(S_FREE(t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status))
+          return false;
+        if (!wait_bounded(K_FULL(t % KS), (t / KS) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + ((t & 1) ? kColS1 : kColS0), base + L::kQ,
+                         base + L::kK + (t % KS) * L::kTile, idesc_rr);
+        return true;
+      };
+      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) && issue_s(0);
+      for (int t = 0; ok && t < n; ++t) {
+        const int s = t % KS;
+        // dP_t = dO V_t^T, once dQ += dS_{t-1} K_{t-1} has read the dP buffer
+        if (t > 0 && !wait_bounded(bar_dq, (t - 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(V_FULL(s), (t / KS) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + kColDP, base + L::kDO, base + L::kV + s * L::kTile, idesc_rr);
+        mma_commit(bar_sdp);     // S_t and dP_t ready
+        mma_commit(V_EMPTY(s));
+        if (t + 1 < n && !issue_s(t + 1)) break;  // overlaps the elementwise step of tile t
+        if (!wait_bounded(bar_ds, t & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        mma_tmem_rows(tmem + kColDQ, tmem + kColDP, base + L::kK + s * L::kTile, idesc_tr, t > 0);
+        mma_commit(bar_dq);
+        mma_commit(K_EMPTY(s));
+      }
+      mma_commit(bar_drain);
+      wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise (thread = query)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int row = qt * kBT + r;
+    const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const size_t vec = static_cast<size_t>(bh) * p.nqp + row;
+    const float lse2 = p.lse2[vec];
+    const float dr = p.dvec[vec];
+    const float sl2 = p.sl2, scale = p.scale;
+    int lim = p.causal ? row + (p.N_kv - p.N_q) : p.N_kv - 1;  // last visible key of this row
+    if (lim > p.N_kv - 1) lim = p.N_kv - 1;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      if (!ew_wait(bar_sdp, t & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t s_col = (t & 1) ? kColS1 : kColS0;
+      const bool masked = t >= first_masked;
+      const int rel = lim - t * kBT;
+#pragma unroll 1
+      for (int c4 = 0; c4 < kBT / 32; ++c4) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(row_tmem + s_col + c4 * 32, sv);
+        tmem_ld32(row_tmem + kColDP + c4 * 32, dpv);
+        tmem_wait_ld();
+        uint32_t dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int c = c4 * 32 + e;
+          const float pa = (!masked || c <= rel) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.0f;
+          const float pb = (!masked || c + 1 <= rel) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.0f;
+          dd[e >> 1] = pack2<BF16>(pa * (__uint_as_float(dpv[e]) - dr) * scale,
+                                   pb * (__uint_as_float(dpv[e + 1]) - dr) * scale);
+        }
+        tmem_st16(row_tmem + kColDP + c4 * 16, dd);  // in place over dP chunks already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(S_FREE(t & 1));
+      mbar_arrive(bar_ds);
+    }
+    if (ok && n > 0) ok = ew_wait(bar_dq, (n - 1) & 1, abort_flag, p.status);
+    if (ok) {
+      tc_fence_after();
+      const bool store = row < p.N_q;
+      const size_t grow = (static_cast<size_t>(bh) * p.N_q + (store ? row : 0)) * D;
+      if (n > 0)
+        store_acc_row<D, BF16>(row_tmem + kColDQ, p.dq + grow, store);
+      else if (store)
+        store_zero_row<D>(p.dq + grow);
+    }
+  }
+#undef K_FULL
+#undef K_EMPTY
+#undef V_FULL
+#undef V_EMPTY
+#undef S_FREE
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdIssuerWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// launcher
+// ------------------------------------------------------------------------------------------
+size_t bwd_workspace_bytes(int B, int Hq, int N_q) {
+  if (B <= 0 || Hq <= 0 || N_q <= 0) return 0;
+  const size_t nqp = (static_cast<size_t>(N_q) + kBT - 1) / kBT * kBT;
+  return static_cast<size_t>(B) * Hq * nqp * 8;  // L log2(e) and D, fp32
+}
+
+template <int D, bool BF16>
+static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
+  constexpr int QS = (D == 128) ? 2 : 3;
+  constexpr int KS = (D == 128) ? 2 : 3;
+  using LK = KvLayout<D, QS>;
+  using LQ = QLayout<D, KS>;
+  const uint64_t bhq = static_cast<uint64_t>(a.B) * a.Hq;
+  const uint64_t bhk = static_cast<uint64_t>(a.B) * a.Hkv;
+  const uint64_t rb = static_cast<uint64_t>(D) * 2;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_3d(&tq, a.q, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
+      !make_tmap_3d(&tdo, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
+      !make_tmap_3d(&tk, a.k, BF16, D, a.N_kv, bhk, rb, rb * a.N_kv, 64, kBT, 1) ||
+      !make_tmap_3d(&tv, a.v, BF16, D, a.N_kv, bhk, rb, rb * a.N_kv, 64, kBT, 1))
+    return -5;
+  BwdParams p;
+  const int n_qtiles = (a.N_q + kBT - 1) / kBT;
+  const int nqp = n_qtiles * kBT;
+  p.lse2 = static_cast<const float*>(a.workspace);
+  p.dvec = p.lse2 + bhq * nqp;
+  p.dq = static_cast<uint16_t*>(a.dq);
+  p.dk = static_cast<uint16_t*>(a.dk);
+  p.dv = static_cast<uint16_t*>(a.dv);
+  p.status = device_status_ptr();
+  if (!p.status) return -5;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.N_q = a.N_q;
+  p.N_kv = a.N_kv;
+  p.n_qtiles = n_qtiles;
+  p.n_kvtiles = (a.N_kv + kBT - 1) / kBT;
+  p.nqp = nqp;
+  p.causal = a.causal;
+  p.scale = a.scale;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  const long long rows = static_cast<long long>(bhq) * nqp;
+  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse,
+      const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), a.N_q, nqp, rows);
+  if (cudaGetLastError() != cudaSuccess) return -5;
+  auto kkv = attn_bwd_dkdv_kernel<D, BF16, QS>;
+  auto kq = attn_bwd_dq_kernel<D, BF16, KS>;
+  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, LK::kBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kBytes) != cudaSuccess)
+    return -5;
+  const uint64_t kv_blocks = bhk * p.n_kvtiles;
+  const uint64_t q_blocks = bhq * n_qtiles;
+  if (kv_blocks > 0x7fffffffull || q_blocks > 0x7fffffffull) return -2;
+  kkv<<<static_cast<unsigned>(kv_blocks), kBwdThreads, LK::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  if (cudaGetLastError() != cudaSuccess) return -5;
+  kq<<<static_cast<unsigned>(q_blocks), kBwdThreads, LQ::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64)
+    return a.bf16 ? launch_bwd_variant<64, true>(a, stream) : launch_bwd_variant<64, false>(a, stream);
+  if (a.d == 128)
+    return a.bf16 ? launch_bwd_variant<128, true>(a, stream) : launch_bwd_variant<128, false>(a, stream);
+  return -2;
+}
+
+}  // namespace attn

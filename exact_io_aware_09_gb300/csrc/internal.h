@@ -113,9 +113,27 @@ struct DecodeArgs {
   int page_size = 0, max_pages = 0, num_pages = 0;
 };
 
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, Hq, Hkv, N_q, N_kv, d, causal;
+  float scale;
+  bool bf16;
+  void* workspace;
+};
+
 // Launchers (return an attn_status_t value).
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
+int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+size_t bwd_workspace_bytes(int B, int Hq, int N_q);
 size_t decode_workspace_bytes(int B, int Hq, int max_seqlen, int split, int d);
 // Device address and size of the library-owned decode scratch of the current device
 // (set up on the first call per device).  Returns 0 or an attn_status_t value.

@@ -90,6 +90,35 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              attn_dtype_t dtype);
 
 /*
+ * attn_bwd_workspace_bytes -- bytes of the workspace attn_bwd needs: two fp32 values (L log2 e
+ * and D) per query row, rounded up to whole 128-row tiles.  0 for invalid arguments.
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N_q);
+
+/*
+ * attn_bwd -- gradients of attn_fwd by recomputation ("FlashAttention Explained", section
+ * "Backward Pass: Recomputation Beats Storage"): with P = exp(scale Q K^T + mask - L),
+ *   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D) with D_i = rowsum(dO_i o O_i),
+ *   dQ = scale dS K,  dK = scale dS^T Q
+ * (grouped-query heads: dK, dV of a key/value head sum over its query heads).
+ *
+ *   q, o, dout   [B, Hq, N_q, d] device, contiguous, 16-bit (`dtype`): the forward's inputs, its
+ *                output O and the incoming gradient dO
+ *   k, v         [B, Hkv, N_kv, d] device
+ *   lse          [B, Hq, N_q] fp32 device: the forward's L (natural log), as attn_fwd returns it
+ *   dq           [B, Hq, N_q, d] out;  dk, dv [B, Hkv, N_kv, d] out; 16-bit `dtype`, written in
+ *                full (no accumulation into them)
+ *   causal, scale, dtype, d (64 or 128)   as the forward call
+ *   workspace    device, >= attn_bwd_workspace_bytes(B, Hq, N_q) bytes, caller-owned scratch
+ * Deterministic: every output element is written by one thread block, without atomics.
+ * Enqueued on `stream`; returns ATTN_OK or a negative attn_status_t.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N_q,
+             int N_kv, int d, int causal, float scale, attn_dtype_t dtype, void *workspace,
+             size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_fwd_window -- prefill attention with a sliding window, the mask that changes the
  * operator ("FlashAttention Explained", FlexAttention section, sliding_causal: key kv is visible
  * to query q iff q >= kv and q - kv <= W; "FlashAttention, annotated", section on causal masks

@@ -64,6 +64,8 @@ def _load():
         lib.oracle_attention_rows_masked.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                      i32, i64, P, i32, f64, P, i64, P, P, i32]
         lib.oracle_attention_rows_masked.restype = i32
+        lib.oracle_round_to_storage.argtypes = [P, P, i64, i32]
+        lib.oracle_round_to_storage.restype = None
         lib.oracle_decode_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, i64,
                                            P, P, i32]
         lib.oracle_decode_rows.restype = i32
@@ -113,6 +115,14 @@ def double_to_f16(x: float) -> int:
 
 def double_to_bf16(x: float) -> int:
     return int(_load().oracle_double_to_bf16(float(x)))
+
+
+def round_to_storage(x: np.ndarray, dtype) -> np.ndarray:
+    """Storage bits of x rounded to fp16 / bf16 (nearest, ties to even)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_round_to_storage(_ptr(x), _ptr(out), x.size, _DT[dtype])
+    return out
 
 
 def bits_to_double(bits: np.ndarray, dtype) -> np.ndarray:

@@ -181,6 +181,12 @@ static void softmax_pv_row_d(const double *s, double *p, int64_t n, const double
     *lse = m + log(l);
 }
 
+/* Round n doubles to the storage type (nearest, ties to even), with the conversions above. */
+void oracle_round_to_storage(const double *x, uint16_t *out, int64_t n, int dtype) {
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = dtype == ORACLE_BF16 ? oracle_double_to_bf16(x[i]) : oracle_double_to_f16(x[i]);
+}
+
 /*
  * Prefill attention for selected rows.  Layouts (contiguous, as on the CUDA side):
  *   q [B, Hq, Nq, d], k/v [B, Hkv, Nkv, d], storage bits of fp16 (dtype 0) or bf16 (1).

@@ -31,7 +31,8 @@ def test_gradients_match_finite_differences_of_the_forward(causal, G):
     """Central differences over one fp16 ulp of an input element (exactly representable
     neighbours), through the C forward oracle, against the analytic gradients."""
     cfg, q, k, v, do = _inputs(1, 2 * G, 2, 5, 7, 4, 40 + G, F16, causal)
-    dq, dk, dv, _, _ = attention_backward(q, k, v, do, F16, 1, 2 * G, 2, 5, 7, 4, causal, cfg.scale)
+    dq, dk, dv, _, _ = attention_backward(q, k, v, do, F16, 1, 2 * G, 2, 5, 7, 4, causal, cfg.scale,
+                                          exact_o=True)
     dod = oracle.bits_to_double(do, F16)
     grads = {"q": dq, "k": dk, "v": dv}
     arrays = {"q": q, "k": k, "v": v}
@@ -78,13 +79,14 @@ def test_softmax_jacobian_invariants(causal):
     dS sums to zero: sum_j dK_j = 0, and with equal key rows dQ = 0."""
     cfg, q, k, v, do = _inputs(1, 2, 2, 40, 40, 16, 70 + causal, BF16, causal)
     dq, dk, dv, _, lse = attention_backward(q, k, v, do, BF16, 1, 2, 2, 40, 40, 16, causal,
-                                            cfg.scale)
+                                            cfg.scale, exact_o=True)
     dod = oracle.bits_to_double(do, BF16).reshape(1, 2, 40, 16)
     live = np.isfinite(lse)[..., None]
     np.testing.assert_allclose(dv.sum(axis=2), (dod * live).sum(axis=2), rtol=0, atol=1e-11)
     np.testing.assert_allclose(dk.sum(axis=2), 0.0, rtol=0, atol=1e-11)
     k[:] = k[:, :, :1, :]
-    dq, _, _, _, _ = attention_backward(q, k, v, do, BF16, 1, 2, 2, 40, 40, 16, causal, cfg.scale)
+    dq, _, _, _, _ = attention_backward(q, k, v, do, BF16, 1, 2, 2, 40, 40, 16, causal, cfg.scale,
+                                        exact_o=True)
     assert np.abs(dq).max() < 1e-12
 
 
@@ -95,3 +97,47 @@ def test_grouped_heads_sum_their_contributions():
              for h in range(4)]
     np.testing.assert_allclose(sum(p[1] for p in parts), dk, rtol=0, atol=1e-12)
     np.testing.assert_allclose(sum(p[2] for p in parts), dv, rtol=0, atol=1e-12)
+
+
+def test_stored_output_changes_only_the_d_term():
+    """D from O rounded to the storage type: dV is unchanged, and dQ, dK move only by the
+    rounding of D (dS changes by -P * dD)."""
+    cfg, q, k, v, do = _inputs(1, 2, 2, 30, 30, 16, 90, BF16, True)
+    ex = attention_backward(q, k, v, do, BF16, 1, 2, 2, 30, 30, 16, True, cfg.scale, exact_o=True)
+    st = attention_backward(q, k, v, do, BF16, 1, 2, 2, 30, 30, 16, True, cfg.scale)
+    np.testing.assert_array_equal(ex[2], st[2])
+    assert 0 < np.abs(ex[0] - st[0]).max() < 1e-2 * np.abs(ex[0]).max()
+    # the rounded O the oracle uses is the storage rounding of its exact O
+    o_bits = oracle.round_to_storage(ex[3], BF16)
+    assert np.abs(oracle.bits_to_double(o_bits, BF16) - ex[3]).max() <= 2.0 ** -8 * np.abs(ex[3]).max()
+
+
+def test_gradient_tolerance_rejects_plausible_mistakes():
+    """The per-row bound used by the GPU parity test (2 x the rounding scales + 1% of the row
+    norm) separates a correct gradient from one with a dropped D term, a missing scale, a
+    transposed dS or a sign error, all planted here in a copy of the oracle's arithmetic."""
+    from oracle.backward import _head_backward
+
+    cfg, q, k, v, do = _inputs(1, 1, 1, 300, 300, 64, 95, BF16, True)
+    qd, kd, vd, dod = (oracle.bits_to_double(x, BF16).reshape(300, 64) for x in (q, k, v, do))
+    dq, dk, dv, o, lse, (eq, ek, ev) = _head_backward(qd, kd, vd, dod, True, cfg.scale,
+                                                      stored_dtype=BF16, unit=2.0 ** -7)
+
+    def passes(got, ref, scales):
+        err = np.linalg.norm(got - ref, axis=1)
+        return bool(np.all(err <= 2.0 * scales + 1e-2 * np.linalg.norm(ref, axis=1) + 1e-6))
+
+    assert passes(dq, dq, eq) and passes(dk, dk, ek) and passes(dv, dv, ev)
+    # the same algebra with one planted mistake each
+    s = cfg.scale * (qd @ kd.T)
+    i = np.arange(300)[:, None]
+    s = np.where(np.arange(300)[None, :] <= i, s, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    dp = dod @ vd.T
+    D = (dod * o).sum(axis=1, keepdims=True)
+    assert not passes(cfg.scale * ((p * dp) @ kd), dq, eq)                    # D dropped
+    assert not passes((p * (dp - D)) @ kd, dq, eq)                             # scale missing
+    assert not passes(cfg.scale * ((p * (D - dp)) @ kd), dq, eq)               # sign of dS
+    assert not passes(cfg.scale * ((p * (dp - D)) @ qd), dk, ek)               # dS not transposed
+    assert not passes(p @ dod, dv, ev)                                         # P instead of P^T
