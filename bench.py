@@ -450,6 +450,17 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
         "block_sparse": lambda: attn.attn_fwd_block_sparse(q, k, v, mask, causal=True, o=o, lse=lse,
                                                            scale=pcfg.scale, stream=stream),
     }
+    # backward of the same prefill: dO drawn on the device, the forward's own O and L
+    dout = torch.randn(q.shape, device=q.device, generator=torch.Generator(q.device).manual_seed(77),
+                       dtype=torch.float32).to(q.dtype)
+    attn.attn_fwd(q, k, v, o=o, lse=lse, causal=True, scale=pcfg.scale, stream=stream)
+    dq_b, dk_b, dv_b = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_b = torch.empty(max(1, attn.attn_bwd_workspace_bytes(pcfg.B, pcfg.Hq, pcfg.N_q)),
+                       device=q.device, dtype=torch.uint8)
+    o_fwd, lse_fwd = o.clone(), lse.clone()
+    calls["backward"] = lambda: attn.attn_bwd(q, k, v, o_fwd, dout, lse_fwd, causal=True,
+                                              scale=pcfg.scale, dq=dq_b, dk=dk_b, dv=dv_b,
+                                              workspace=ws_b, stream=stream)
     out = {}
     for name, fn in calls.items():
         for _ in range(3):
@@ -465,11 +476,18 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
         if st != 0:
             raise SystemExit(f"device status after {name}: {attn.attn_status_string(st)}")
         ms = e0.elapsed_time(e1) / args.steps
-        flops = 4.0 * pcfg.d * float(per_head[name]) * pcfg.B * pcfg.Hq
+        if name == "backward":
+            # the pages' count: five matmuls against the forward's two (2.5x its FLOPs)
+            flops = 2.5 * pcfg.flops()
+        else:
+            flops = 4.0 * pcfg.d * float(per_head[name]) * pcfg.B * pcfg.Hq
         tf = flops / (ms / 1e3) / 1e12
         out[name] = {
             "workload": (f"sliding window W={W}" if name == "window" else
-                         f"causal block pattern, {int(pattern.sum())} of {pattern.size} blocks")
+                         f"causal block pattern, {int(pattern.sum())} of {pattern.size} blocks"
+                         if name == "block_sparse" else
+                         "backward (dQ, dK, dV) of the causal GQA prefill, FLOPs by the pages' "
+                         "5-matmul count (2.5x forward); 3 launches")
                         + " on the prefill workload's inputs",
             "ms_per_launch": round(ms, 4), "flops_per_launch": flops, "value": round(tf, 1),
             "unit": "TFLOP/s",

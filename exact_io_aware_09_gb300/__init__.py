@@ -162,6 +162,10 @@ def _fwd_prep(q, k, v, o, lse, scale):
     return B, Hq, Hkv, N_q, N_kv, d, o, lse, float(scale)
 
 
+def attn_bwd_workspace_bytes(B: int, Hq: int, N_q: int) -> int:
+    return int(lib.attn_bwd_workspace_bytes(B, Hq, N_q))
+
+
 def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
              dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Gradients (dq, dk, dv) of attn_fwd for the incoming gradient ``dout`` (shape of o).

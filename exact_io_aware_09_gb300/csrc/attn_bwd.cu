@@ -160,8 +160,9 @@ struct KvLayout {
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
-  // kv_full, st_full[QS], st_empty[QS], sdp_full, pds_ready, mm_done, drain
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 4;
+  // kv_full, st_full[QS], st_empty[QS], s_full, dp_full, p_ready, ds_ready, p_done, ds_done,
+  // drain
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 7;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tile alignment");
@@ -183,18 +184,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_kv = bars;
 #define ST_FULL(s) (bars + 8u * (1 + (s)))
 #define ST_EMPTY(s) (bars + 8u * (1 + QS + (s)))
-  const uint32_t bar_sdp = bars + 8u * (1 + 2 * QS);
-  const uint32_t bar_pds = bar_sdp + 8;
-  const uint32_t bar_mm = bar_sdp + 16;
-  const uint32_t bar_drain = bar_sdp + 24;
+  const uint32_t bar_s = bars + 8u * (1 + 2 * QS);  // S^T_i written (MMA commit)
+  const uint32_t bar_dp = bar_s + 8;                 // dP^T_i written (MMA commit)
+  const uint32_t bar_p = bar_s + 16;                 // P^T_i stored over S^T (128 arrivals)
+  const uint32_t bar_ds = bar_s + 24;                // dS^T_i stored over dP^T (128 arrivals)
+  const uint32_t bar_pdone = bar_s + 32;             // dV += P^T_i dO_i finished: S^T free
+  const uint32_t bar_dsdone = bar_s + 40;            // dK += dS^T_i Q_i finished: dP^T free
+  const uint32_t bar_drain = bar_s + 48;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // item: key tile kt of (batch, key/value head) bkv; small kt first (most query tiles)
-  const int bkv = blockIdx.x / p.n_kvtiles;
-  const int kt = static_cast<int>(blockIdx.x % p.n_kvtiles);
+  // item: key tile kt of (batch, key/value head) bkv
+  // key tile major: under the causal mask the first key tiles have the most query tiles, so
+  // every (batch, key/value head)'s longest items start first
+  const int n_planes = static_cast<int>(gridDim.x / p.n_kvtiles);
+  const int kt = static_cast<int>(blockIdx.x / n_planes);
+  const int bkv = static_cast<int>(blockIdx.x % n_planes);
   const int b = bkv / p.Hkv;
   const int hk = bkv % p.Hkv;
   const int off = p.N_kv - p.N_q;
@@ -212,9 +219,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(ST_FULL(s), 1);
       mbar_init(ST_EMPTY(s), 1);
     }
-    mbar_init(bar_sdp, 1);
-    mbar_init(bar_pds, kEwThreads);
-    mbar_init(bar_mm, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_p, kEwThreads);
+    mbar_init(bar_ds, kEwThreads);
+    mbar_init(bar_pdone, 1);
+    mbar_init(bar_dsdone, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -269,23 +279,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
       constexpr uint32_t idesc_tr = make_idesc_f16(BF16, kBT, D, true);
-      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status);
+      // Per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; once P^T_i is stored,
+      // dV += P^T_i dO_i; once dS^T_i is stored, dK += dS^T_i Q_i.  The next tile's S^T waits
+      // only for the dV MMA (which read P^T over S^T) and its dP^T for the dK MMA, so the tensor
+      // pipe runs dV_i, dK_i, S^T_{i+1}, dP^T_{i+1} back to back while the elementwise warps
+      // work on the other half of the tile pair.
+      auto issue_sdp = [&](int i) -> bool {
+        const int s = i % QS;
+        const uint32_t st = base + L::kStages + s * L::kStage;
+        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
+        if (i > 0 && !wait_bounded(bar_pdone, (i - 1) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + kColS, base + L::kK, st, idesc_rr);  // S^T = K Q^T
+        mma_commit(bar_s);
+        if (i > 0 && !wait_bounded(bar_dsdone, (i - 1) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + kColDP, base + L::kV, st + L::kTile, idesc_rr);  // dP^T = V dO^T
+        mma_commit(bar_dp);
+        return true;
+      };
+      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_sdp(0);
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % QS;
         const uint32_t st = base + L::kStages + s * L::kStage;
-        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) break;
-        // S^T and dP^T of the previous tile were read as A operands by its last MMAs
-        if (i > 0 && !wait_bounded(bar_mm, (i - 1) & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        mma_rows_rows<D>(tmem + kColS, base + L::kK, st, idesc_rr);               // S^T = K Q^T
-        mma_rows_rows<D>(tmem + kColDP, base + L::kV, st + L::kTile, idesc_rr);   // dP^T = V dO^T
-        mma_commit(bar_sdp);
-        if (!wait_bounded(bar_pds, i & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(bar_p, i & 1, abort_flag, p.status)) break;
         tc_fence_after();
         mma_tmem_rows(tmem + kColDV, tmem + kColS, st + L::kTile, idesc_tr, i > 0);  // dV += P^T dO
-        mma_tmem_rows(tmem + kColDK, tmem + kColDP, st, idesc_tr, i > 0);           // dK += dS^T Q
-        mma_commit(bar_mm);
+        mma_commit(bar_pdone);
+        if (!wait_bounded(bar_ds, i & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        mma_tmem_rows(tmem + kColDK, tmem + kColDP, st, idesc_tr, i > 0);  // dK += dS^T Q
+        mma_commit(bar_dsdone);
         mma_commit(ST_EMPTY(s));
+        if (i + 1 < n) ok = issue_sdp(i + 1);
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -304,47 +330,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int qt = qt_lo + i % nq_per;
       const float* lv = reinterpret_cast<const float*>(gbase + L::kStages + s * L::kStage + 2 * L::kTile);
       const float* dvv = lv + kBT;
-      if (!ew_wait(bar_sdp, i & 1, abort_flag, p.status)) {
+      const int q_first_visible = kr - off;  // the smallest query row that sees this key
+      // P^T row of this key over the tile's 128 queries, kept in registers for dS^T
+      float pv[kBT];
+      if (!ew_wait(bar_s, i & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // keys above this bound are masked for query row q: key <= q + off
-      const int q_first_visible = kr - off;  // the smallest query row that sees this key
-#pragma unroll 1
+#pragma unroll
       for (int c4 = 0; c4 < kBT / 32; ++c4) {
-        uint32_t sv[32], dpv[32];
+        uint32_t sv[32];
         tmem_ld32(row_tmem + kColS + c4 * 32, sv);
+        tmem_wait_ld();
+        uint32_t pp[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int col = c4 * 32 + e;
+          const float4 l4 = *reinterpret_cast<const float4*>(lv + col);
+          const int qrow = qt * kBT + col;
+          const bool causal = p.causal;
+          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool vis = !causal || qrow + u >= q_first_visible;
+            pv[col + u] = vis ? ex2(fmaf(__uint_as_float(sv[e + u]), sl2, -la[u])) : 0.0f;
+          }
+          pp[(e >> 1)] = pack2<BF16>(pv[col], pv[col + 1]);
+          pp[(e >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
+        }
+        tmem_st16(row_tmem + kColS + c4 * 16, pp);  // in place: chunks already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+      if (!ew_wait(bar_dp, i & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < kBT / 32; ++c4) {
+        uint32_t dpv[32];
         tmem_ld32(row_tmem + kColDP + c4 * 32, dpv);
         tmem_wait_ld();
-        uint32_t pp[16], dd[16];
+        uint32_t dd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 32; e += 4) {
           const int col = c4 * 32 + e;
-          const int qrow = qt * kBT + col;
-          const float4 l4 = *reinterpret_cast<const float4*>(lv + (col & ~3));
-          const float4 d4 = *reinterpret_cast<const float4*>(dvv + (col & ~3));
-          const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
-          const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
-          const bool va = !p.causal || qrow >= q_first_visible;
-          const bool vb = !p.causal || qrow + 1 >= q_first_visible;
-          const float pa = va ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -la)) : 0.0f;
-          const float pb = vb ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lb)) : 0.0f;
-          const float dsa = pa * (__uint_as_float(dpv[e]) - da) * scale;
-          const float dsb = pb * (__uint_as_float(dpv[e + 1]) - db) * scale;
-          pp[e >> 1] = pack2<BF16>(pa, pb);
-          dd[e >> 1] = pack2<BF16>(dsa, dsb);
+          const float4 d4 = *reinterpret_cast<const float4*>(dvv + col);
+          dd[e >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[e]) - d4.x) * scale,
+                                   pv[col + 1] * (__uint_as_float(dpv[e + 1]) - d4.y) * scale);
+          dd[(e >> 1) + 1] = pack2<BF16>(pv[col + 2] * (__uint_as_float(dpv[e + 2]) - d4.z) * scale,
+                                         pv[col + 3] * (__uint_as_float(dpv[e + 3]) - d4.w) * scale);
         }
-        // in place: these columns belong to chunks already read
-        tmem_st16(row_tmem + kColS + c4 * 16, pp);
         tmem_st16(row_tmem + kColDP + c4 * 16, dd);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_pds);
+      mbar_arrive(bar_ds);
     }
     // epilogue: dV and dK rows of this key tile
-    if (ok && n > 0) ok = ew_wait(bar_mm, (n - 1) & 1, abort_flag, p.status);
+    // the last dK MMA finished means every MMA of the block has (they complete in issue order)
+    if (ok && n > 0) ok = ew_wait(bar_dsdone, (n - 1) & 1, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const bool store = kr < p.N_kv;
