@@ -1,0 +1,174 @@
+"""Oracle of the FP8 forward with incoherent processing (TEST INFRASTRUCTURE ONLY).
+
+Only the test suite, the smoke check and the CPU-baseline leg of the benchmark use this
+module; the CUDA library shares nothing with it.
+
+"FlashAttention Explained", section "FP8 Attention and Incoherent Processing": Q and K are
+multiplied by the same random orthogonal matrix M before quantisation, so that
+(Q M)(K M)^T = Q K^T while outlier channels spread over all channels; M is a Hadamard transform
+with random sign flips; the inputs are quantised to E4M3 with per-block scaling factors.
+
+Steps, each written out here:
+  1. M = H diag(s) / sqrt(d): x -> H (s o x) / sqrt(d), H the Sylvester Hadamard matrix applied
+     by the fast Walsh-Hadamard butterflies (stage h = 1, 2, 4, ..., d/2: (a, b) -> (a + b,
+     a - b) on elements j and j + h), in fp32 in that order, then one fp32 multiply by the fp32
+     value of 1/sqrt(d).  The rotation decides integer codes below, so it is evaluated in the
+     precision and order the kernel uses (fp32).
+  2. Block quantisation: one scale per 128-row tile of a (batch, head) plane for Q and K
+     (amax of the tile / 448, the largest E4M3 value) and one per plane for V (not rotated);
+     code = E4M3(x / scale) rounded to nearest even, saturating at +-448.
+  3. Attention in fp64 of the dequantised operands (code value * scale): the same definition as
+     the prefill oracle, on these inputs.
+Readings where the pages are silent (block shape, V's scale, the P conversion of the kernel)
+are listed in the design notes.
+"""
+import numpy as np
+
+E4M3_MAX = 448.0
+
+
+# ------------------------------------------------------------------------------------------
+# E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal
+# (m * 2^-9); exponent 15 with mantissa 7 is NaN (no infinities); largest finite 1.75 * 2^8.
+# ------------------------------------------------------------------------------------------
+def e4m3_decode(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x):
+    """Nearest E4M3 code (ties to even), saturating to +-448; x float32/float64 (exact)."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x)
+    a = np.abs(x)
+    a = np.minimum(a, E4M3_MAX)  # saturating (finite inputs only)
+    # exponent of the normal binade, clamped to the subnormal range
+    _, ex = np.frexp(a)          # a = f * 2^ex, f in [0.5, 1)
+    e_unb = np.maximum(ex - 1, -6)   # binade [2^e, 2^(e+1)); below 2^-6 the spacing is 2^-9
+    step = np.exp2(e_unb.astype(np.float64) - 3)  # spacing of representable values
+    q = a / step                      # exact (power-of-two scaling)
+    r = np.floor(q)
+    frac = q - r
+    up = (frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1))
+    r = r + up
+    v = r * step                      # rounded magnitude (may reach the next binade: still exact)
+    v = np.minimum(v, E4M3_MAX)
+    # back to bits
+    _, ev = np.frexp(v)
+    e_v = np.maximum(ev - 1, -6)
+    is_sub = (v < 2.0 ** -6)
+    m_sub = np.round(v / 2.0 ** -9).astype(np.int64)
+    m_nrm = np.round((v / np.exp2(e_v.astype(np.float64)) - 1.0) * 8).astype(np.int64)
+    e_field = np.where(is_sub, 0, e_v + 7)
+    m_field = np.where(is_sub, m_sub, m_nrm)
+    code = (e_field.astype(np.int64) << 3) | m_field
+    code = np.where(v == 0, 0, code)
+    return (code | np.where(sign, 0x80, 0)).astype(np.uint8)
+
+
+# ------------------------------------------------------------------------------------------
+# rotation and quantisation
+# ------------------------------------------------------------------------------------------
+def rotate_f32(x, signs):
+    """Rows of x (float32 [..., d]) -> H (s o x) / sqrt(d) in fp32, butterflies in order."""
+    y = np.asarray(x, dtype=np.float32) * np.asarray(signs, dtype=np.float32)
+    d = y.shape[-1]
+    y = y.copy()
+    h = 1
+    while h < d:
+        y = y.reshape(y.shape[:-1] + (d // (2 * h), 2, h))
+        a = y[..., 0, :].copy()
+        b = y[..., 1, :].copy()
+        y[..., 0, :] = a + b
+        y[..., 1, :] = a - b
+        y = y.reshape(y.shape[:-3] + (d,))
+        h *= 2
+    return y * np.float32(1.0 / np.sqrt(np.float32(d)))
+
+
+def quantize_tiles(x, rows_per_tile=128):
+    """x float32 [planes, N, d] -> (codes uint8 [planes, N, d], scales float32 [planes, tiles]).
+    One scale per 128-row tile: amax / 448 (1 for an all-zero tile); codes = E4M3(x / scale),
+    the division in fp32."""
+    x = np.asarray(x, dtype=np.float32)
+    P, N, d = x.shape
+    nt = -(-N // rows_per_tile)
+    codes = np.zeros((P, N, d), dtype=np.uint8)
+    scales = np.ones((P, nt), dtype=np.float32)
+    for t in range(nt):
+        blk = x[:, t * rows_per_tile:(t + 1) * rows_per_tile]
+        amax = np.abs(blk).reshape(P, -1).max(axis=1)
+        sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        scales[:, t] = sc
+        codes[:, t * rows_per_tile:(t + 1) * rows_per_tile] = e4m3_encode(
+            (blk / sc[:, None, None]).astype(np.float32))
+    return codes, scales
+
+
+def quantize_planes(x):
+    """x float32 [planes, N, d] -> (codes, scales [planes]): one scale per plane."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x).reshape(x.shape[0], -1).max(axis=1) if x.size else np.zeros(x.shape[0])
+    sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    return e4m3_encode((x / sc[:, None, None]).astype(np.float32)), sc
+
+
+def prepare(q, k, v, signs):
+    """float32 q [B, Hq, Nq, d], k/v [B, Hkv, Nkv, d] and signs [d] (None: no rotation) ->
+    the quantised operands and their scales, as the kernel's preparation writes them."""
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    qr = rotate_f32(q, signs) if signs is not None else np.asarray(q, np.float32)
+    kr = rotate_f32(k, signs) if signs is not None else np.asarray(k, np.float32)
+    q8, sq = quantize_tiles(qr.reshape(B * Hq, Nq, d))
+    k8, sk = quantize_tiles(kr.reshape(B * Hkv, Nkv, d))
+    v8, sv = quantize_planes(np.asarray(v, np.float32).reshape(B * Hkv, Nkv, d))
+    return dict(q8=q8, sq=sq, k8=k8, sk=sk, v8=v8, sv=sv)
+
+
+def dequantized(prep, B, Hq, Hkv, Nq, Nkv, d):
+    """fp64 values the FP8 kernel multiplies: code value times its block's scale."""
+    qd = e4m3_decode(prep["q8"]) * np.repeat(prep["sq"], 128, axis=1)[:, :Nq, None]
+    kd = e4m3_decode(prep["k8"]) * np.repeat(prep["sk"], 128, axis=1)[:, :Nkv, None]
+    vd = e4m3_decode(prep["v8"]) * prep["sv"][:, None, None].astype(np.float64)
+    return qd.reshape(B, Hq, Nq, d), kd.reshape(B, Hkv, Nkv, d), vd.reshape(B, Hkv, Nkv, d)
+
+
+def attention_f64(q, k, v, causal, scale):
+    """fp64 attention of arbitrary fp64 operands q [B,Hq,Nq,d], k/v [B,Hkv,Nkv,d] (numpy matmul
+    per head; the same masking and empty-row rule as the prefill oracle) -> (o, lse)."""
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    o = np.zeros((B, Hq, Nq, d))
+    lse = np.full((B, Hq, Nq), -np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * (q[b, h] @ k[b, h // G].T)
+            if causal:
+                i = np.arange(Nq)[:, None] + (Nkv - Nq)
+                s = np.where(np.arange(Nkv)[None, :] <= i, s, -np.inf)
+            m = s.max(axis=1) if Nkv else np.full(Nq, -np.inf)
+            live = np.isfinite(m)
+            e = np.where(live[:, None], np.exp(s - np.where(live, m, 0.0)[:, None]), 0.0)
+            l = e.sum(axis=1)
+            o[b, h] = np.where(live[:, None], (e @ v[b, h // G]) / np.where(l > 0, l, 1.0)[:, None],
+                               0.0)
+            lse[b, h] = np.where(live, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def fp8_attention(q, k, v, signs, causal, scale):
+    """The FP8 forward's reference: exact attention of the dequantised rotated operands.
+    q, k, v float32 (the 16-bit inputs' values).  Returns (o, lse, prep)."""
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    prep = prepare(q, k, v, signs)
+    qd, kd, vd = dequantized(prep, B, Hq, Hkv, Nq, Nkv, d)
+    o, lse = attention_f64(qd, kd, vd, causal, scale)
+    return o, lse, prep

@@ -1,0 +1,100 @@
+"""Pins of the FP8 oracle (oracle/fp8.py): the E4M3 codec against the format's definition and
+an independent library conversion, the signed Hadamard rotation against a library Hadamard
+matrix and orthogonality, and the fp64 attention against the pinned prefill oracle
+("FlashAttention Explained", section "FP8 Attention and Incoherent Processing")."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from oracle import fp8
+
+
+def test_e4m3_decode_fixed_points():
+    dec = fp8.e4m3_decode
+    assert dec(0x7E) == 448.0 and dec(0xFE) == -448.0      # largest finite
+    assert dec(0x38) == 1.0 and dec(0x08) == 2.0 ** -6     # one, smallest normal
+    assert dec(0x01) == 2.0 ** -9 and dec(0x07) == 7 * 2.0 ** -9   # subnormals
+    assert dec(0x39) == 1.125 and dec(0x3F) == 1.875
+    assert np.isnan(dec(0x7F)) and np.isnan(dec(0xFF))
+    assert dec(0x00) == 0.0
+
+
+def test_e4m3_encode_round_trips_every_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    np.testing.assert_array_equal(fp8.e4m3_encode(fp8.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_encode_ties_to_even_and_saturates():
+    enc = fp8.e4m3_encode
+    assert enc(1.0625) == 0x38       # halfway 1.0 / 1.125 -> even mantissa (1.0)
+    assert enc(1.1875) == 0x3A       # halfway 1.125 / 1.25 -> 1.25
+    assert enc(1.0626) == 0x39
+    assert enc(2.0 ** -10) == 0x00   # halfway 0 / 2^-9 -> 0
+    assert enc(3 * 2.0 ** -10) == 0x02
+    assert enc(1000.0) == 0x7E and enc(-1e9) == 0xFE
+    assert enc(464.0) == 0x7E
+
+
+def test_e4m3_encode_matches_an_independent_conversion():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.uniform(-3, 2.5, 20000)).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(fp8.e4m3_encode(x), ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_rotation_is_the_signed_hadamard_matrix(d):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    H = scipy_linalg.hadamard(d) / np.sqrt(d)
+    signs = np.where(np.random.default_rng(d).random(d) < 0.5, -1.0, 1.0)
+    eye = np.eye(d, dtype=np.float32)
+    M = fp8.rotate_f32(eye, signs).astype(np.float64)   # row i = M applied to e_i
+    np.testing.assert_allclose(M, (H @ np.diag(signs)).T, rtol=0, atol=2e-7)
+    np.testing.assert_allclose(M @ M.T, np.eye(d), rtol=0, atol=1e-6)
+    x = np.random.default_rng(1).standard_normal((5, d)).astype(np.float32)
+    y = np.random.default_rng(2).standard_normal((7, d)).astype(np.float32)
+    np.testing.assert_allclose(fp8.rotate_f32(x, signs) @ fp8.rotate_f32(y, signs).T, x @ y.T,
+                               rtol=0, atol=5e-5)
+
+
+def test_quantisation_error_is_at_most_half_a_step():
+    x = np.random.default_rng(4).standard_normal((3, 300, 128)).astype(np.float32)
+    x[0, 5, 7] = 60.0  # an outlier sets its tile's scale
+    codes, scales = fp8.quantize_tiles(x)
+    for t in range(3):
+        blk = x[:, t * 128:(t + 1) * 128] / scales[:, t][:, None, None]
+        deq = fp8.e4m3_decode(codes[:, t * 128:(t + 1) * 128])
+        a = np.abs(blk).astype(np.float64)
+        step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(a, 1e-30))), -6) - 3)
+        assert np.all(np.abs(deq - blk) <= step / 2 + 1e-12)
+    # the tile holding the outlier reaches the top of the E4M3 range exactly
+    assert np.abs(fp8.e4m3_decode(codes[0, :128])).max() == 448.0
+
+
+def test_f64_attention_matches_the_prefill_oracle():
+    cfg = syn.PrefillConfig("f8", 1, 4, 2, 70, 90, 32, "bf16", True, 55)
+    q, k, v = cfg.host_inputs()
+    qx, kx, vx = (oracle.bits_to_double(t, "bf16") for t in (q, k, v))
+    o, lse = fp8.attention_f64(qx, kx, vx, True, cfg.scale)
+    of, lf = oracle.attention(q, k, v, "bf16", 1, 4, 2, 70, 90, 32, True, cfg.scale)
+    np.testing.assert_allclose(o, of, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lf, rtol=0, atol=1e-12)
+
+
+def test_rotation_leaves_unquantised_scores_unchanged():
+    """(Q M)(K M)^T = Q K^T: without quantisation the rotated problem is the same attention."""
+    cfg = syn.PrefillConfig("f8", 1, 2, 1, 40, 40, 64, "bf16", False, 56)
+    q, k, v = cfg.host_inputs()
+    qx, kx, vx = (oracle.bits_to_double(t, "bf16") for t in (q, k, v))
+    signs = np.where(np.random.default_rng(0).random(64) < 0.5, -1.0, 1.0)
+    qr = fp8.rotate_f32(qx.astype(np.float32), signs).astype(np.float64)
+    kr = fp8.rotate_f32(kx.astype(np.float32), signs).astype(np.float64)
+    o1, l1 = fp8.attention_f64(qx, kx, vx, False, cfg.scale)
+    o2, l2 = fp8.attention_f64(qr, kr, vx, False, cfg.scale)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-5)
