@@ -461,6 +461,15 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
     calls["backward"] = lambda: attn.attn_bwd(q, k, v, o_fwd, dout, lse_fwd, causal=True,
                                               scale=pcfg.scale, dq=dq_b, dk=dk_b, dv=dv_b,
                                               workspace=ws_b, stream=stream)
+    # FP8 with incoherent processing: rotation, block quantisation and attention per launch
+    import synthetic as syn
+
+    signs = torch.from_numpy(syn.random_signs(pcfg.d, 79)).to(q.device)
+    ws_f8 = torch.empty(attn.attn_fwd_fp8_workspace_bytes(pcfg.B, pcfg.Hq, pcfg.Hkv, pcfg.N_q,
+                                                          pcfg.N_kv, pcfg.d),
+                        device=q.device, dtype=torch.uint8)
+    calls["fp8"] = lambda: attn.attn_fwd_fp8(q, k, v, signs, o=o, lse=lse, causal=True,
+                                             scale=pcfg.scale, workspace=ws_f8, stream=stream)
     out = {}
     for name, fn in calls.items():
         for _ in range(3):
@@ -476,9 +485,14 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
         if st != 0:
             raise SystemExit(f"device status after {name}: {attn.attn_status_string(st)}")
         ms = e0.elapsed_time(e1) / args.steps
+        peak, peak_note = peaks["bf16_tflops"], f"{peak_src} bf16 burst (cuBLAS)"
         if name == "backward":
             # the pages' count: five matmuls against the forward's two (2.5x its FLOPs)
             flops = 2.5 * pcfg.flops()
+        elif name == "fp8":
+            flops = pcfg.flops()
+            # E4M3 tensor rate: the bf16 measurement times the nominal ratio 4.5 / 2.25
+            peak, peak_note = 2.0 * peak, f"{peak_src} bf16 burst (cuBLAS) x 2 (nominal fp8/bf16)"
         else:
             flops = 4.0 * pcfg.d * float(per_head[name]) * pcfg.B * pcfg.Hq
         tf = flops / (ms / 1e3) / 1e12
@@ -487,13 +501,14 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
                          f"causal block pattern, {int(pattern.sum())} of {pattern.size} blocks"
                          if name == "block_sparse" else
                          "backward (dQ, dK, dV) of the causal GQA prefill, FLOPs by the pages' "
-                         "5-matmul count (2.5x forward); 3 launches")
+                         "5-matmul count (2.5x forward); 3 launches" if name == "backward" else
+                         "causal prefill in FP8 (E4M3) with a randomised Hadamard rotation of Q "
+                         "and K; each launch includes the rotation and quantisation (5 launches)")
                         + " on the prefill workload's inputs",
             "ms_per_launch": round(ms, 4), "flops_per_launch": flops, "value": round(tf, 1),
             "unit": "TFLOP/s",
-            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
-                         "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
-                         "frac": round(tf / peaks["bf16_tflops"], 4)},
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                         "peak_source": peak_note, "frac": round(tf / peak, 4)},
         }
     return out
 

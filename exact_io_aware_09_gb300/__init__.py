@@ -39,6 +39,12 @@ lib.attn_bwd_workspace_bytes.restype = _SZ
 lib.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
                          _SZ, _P]
 lib.attn_bwd.restype = _I
+lib.attn_fwd_fp8_workspace_bytes.argtypes = [_I] * 6
+lib.attn_fwd_fp8_workspace_bytes.restype = _SZ
+lib.attn_fwd_fp8_workspace_offsets.argtypes = [_I] * 6 + [_P]
+lib.attn_fwd_fp8_workspace_offsets.restype = _I
+lib.attn_fwd_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P, _I]
+lib.attn_fwd_fp8.restype = _I
 lib.attn_fwd_window.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I]
 lib.attn_fwd_window.restype = _I
 lib.attn_fwd_block_sparse.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P,
@@ -196,6 +202,38 @@ def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
                       _dev_ptr(workspace, "workspace"), workspace.numel(), _stream_handle(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d) -> int:
+    return int(lib.attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d))
+
+
+def attn_fwd_fp8_workspace_offsets(B, Hq, Hkv, N_q, N_kv, d):
+    """Byte offsets of (Q codes, K codes, V^T codes, Q scales, K scales, V scales, scratch)."""
+    off = (ctypes.c_size_t * 7)()
+    _check(lib.attn_fwd_fp8_workspace_offsets(B, Hq, Hkv, N_q, N_kv, d, off),
+           "attn_fwd_fp8_workspace_offsets")
+    return list(off)
+
+
+def attn_fwd_fp8(q, k, v, signs=None, o=None, lse=None, causal: bool = False,
+                 scale: float | None = None, workspace=None, stream=None):
+    """FP8 prefill with incoherent processing.  signs: int8 CUDA tensor [d] of +-1 (None: no
+    rotation).  Shapes and return value as attn_fwd (d = 128)."""
+    torch = _torch()
+    B, Hq, Hkv, N_q, N_kv, d, o, lse, scale = _fwd_prep(q, k, v, o, lse, scale)
+    if signs is not None and (signs.dtype != torch.int8 or tuple(signs.shape) != (d,)):
+        raise AttnError(-1, "attn_fwd_fp8: signs must be int8 [d]")
+    if workspace is None:
+        workspace = torch.empty(max(1, attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d)),
+                                device=q.device, dtype=torch.uint8)
+    st = lib.attn_fwd_fp8(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                          _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(bool(causal)), scale,
+                          _dev_ptr(signs, "signs") if signs is not None else None,
+                          _dev_ptr(workspace, "workspace"), workspace.numel(),
+                          _stream_handle(stream), _dtype_code(q))
+    _check(st, "attn_fwd_fp8")
+    return o, lse
 
 
 def attn_fwd_window(q, k, v, window: int, o=None, lse=None, scale: float | None = None,

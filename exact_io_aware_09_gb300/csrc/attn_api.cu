@@ -72,6 +72,22 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                     uint32_t box1, uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || dim0 == 0 || dim1 == 0 || dim2 == 0) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -145,6 +161,43 @@ int attn_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, 
   if (!block_mask) return ATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal, -1, block_mask, scale,
                     stream, dtype);
+}
+
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int N_q, int N_kv, int d) {
+  size_t off[7];
+  return fp8_workspace_layout(B, Hq, Hkv, N_q, N_kv, d, off);
+}
+
+int attn_fwd_fp8_workspace_offsets(int B, int Hq, int Hkv, int N_q, int N_kv, int d,
+                                   size_t* offsets) {
+  if (!offsets) return ATTN_ERR_INVALID_ARG;
+  return fp8_workspace_layout(B, Hq, Hkv, N_q, N_kv, d, offsets) ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N_q, int N_kv, int d, int causal, float scale, const int8_t* signs,
+                 void* workspace, size_t workspace_bytes, attn_stream_t stream,
+                 attn_dtype_t dtype) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N_q < 0 || N_kv < 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || N_q == 0) return ATTN_OK;
+  if (N_kv == 0)  // nothing to quantise: O = 0, L = -inf as in attn_fwd
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal, -1, nullptr, scale,
+                      stream, dtype);
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return ATTN_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d))
+    return ATTN_ERR_WORKSPACE;
+  const int dev_ok = check_device();
+  if (dev_ok != ATTN_OK) return dev_ok;
+  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale,
+            dtype == ATTN_BF16, -1, nullptr};
+  return launch_attn_fwd_fp8(a, signs, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_kv_span(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,

@@ -82,6 +82,11 @@ struct PCols {
   static_assert(kP1 + 64 <= kTmemCols, "tensor memory budget");
 };
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max rises by > 2^8
+// FP8: P enters the P V product as 2^kPShift8 P in E4M3.  The maximum moves whenever it rises by
+// more than 2^kRescaleThreshold8, so P <= 2 and 2^7 P <= 256, inside E4M3's +-448; the row sum
+// carries the same factor, which the epilogue removes.
+constexpr float kRescaleThreshold8 = 1.0f;
+constexpr int kPShift8 = 7;
 constexpr uint32_t kSubTile = 128 * 128;   // bytes of one 64-column, 128-row swizzled sub-tile
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 
@@ -96,6 +101,10 @@ struct FwdParams {
   int window;       // sliding window, keys behind the diagonal (-1: none)
   int n_kvtiles;    // key tiles of the sequence (row length of block_mask)
   const uint8_t* block_mask;  // [query tile][key tile], nonzero = compute; null: every tile
+  // FP8 operands: E4M3 block scales of Q [B*Hq][query tile], K [B*Hkv][key tile], V [B*Hkv]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
   float sl2;  // scale * log2(e)
 };
 
@@ -119,16 +128,18 @@ enum FwdBar : uint32_t {
   kNumFixedBars = 24
 };
 
-template <int D, int KS, int VS>
+template <int D, int KS, int VS, bool FP8 = false>
 struct FwdLayout {
-  static constexpr uint32_t kQBytes = kBlockM * D * 2;
-  static constexpr uint32_t kKVBytes = kBlockN * D * 2;
+  static constexpr uint32_t kElem = FP8 ? 1 : 2;  // bytes per Q/K/V element
+  static constexpr uint32_t kQBytes = kBlockM * D * kElem;
+  static constexpr uint32_t kKVBytes = kBlockN * D * kElem;
+  static constexpr uint32_t kOBytes = kBlockM * D * 2;  // O is written in 16 bits
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kQBytes;          // K ring, KS slots
   static constexpr uint32_t kV = kK + KS * kKVBytes;    // V ring, VS slots
   static constexpr uint32_t kOst = kV + VS * kKVBytes;  // O staging for the TMA store
   // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], then the FwdBar barriers
-  static constexpr uint32_t kBar = kOst + kQBytes;
+  static constexpr uint32_t kBar = kOst + kOBytes;
   static constexpr uint32_t kFixedBar = kBar + 2 * (KS + VS) * 8;
   static constexpr uint32_t kMisc = kFixedBar + kNumFixedBars * 8;  // tmem slot, abort, ring[2]
   static constexpr uint32_t kClc = (kMisc + 16 + 15) & ~15u;        // 16-byte answer
@@ -207,7 +218,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // to the staging buffer of the TMA store (128-byte-swizzled sub-tiles of 64 columns), and
 // L = m + ln l to global memory.  m_fin is the item's final maximum and (l_own, m_own) this
 // warpgroup's partial sum and the maximum it refers to.
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8 = false>
 __device__ __forceinline__ bool run_epilogue(uint32_t o_tmem, float m_fin, float l_own,
                                              float m_own, int item, int q0, int bh, int r,
                                              uint32_t fbars, const float* lpart, uint8_t* staging,
@@ -219,7 +230,10 @@ __device__ __forceinline__ bool run_epilogue(uint32_t o_tmem, float m_fin, float
   float l_row = lpart[slot * kBlockM + r];
   mbar_arrive(fbars + 8u * (kBarLEmpty + slot));
   if (m_own != -INFINITY) l_row += l_own * ex2(m_own - m_fin);
-  const float inv_l = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+  // FP8: the accumulator holds sum_j (2^7 p_j)_E4M3 v8_j with V = v8 * v_scale
+  float out_scale = 1.0f;
+  if constexpr (FP8) out_scale = p.v_scale[(bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group];
+  const float inv_l = (l_row > 0.0f) ? out_scale / l_row : 0.0f;
   if (item >= 1 && !warp_wait(fbars + 8u * kBarOStage, (item - 1) & 1, abort_flag, p.status))
     return false;
 #pragma unroll 1
@@ -247,19 +261,22 @@ __device__ __forceinline__ bool run_epilogue(uint32_t o_tmem, float m_fin, float
   const int row = q0 + r;
   if (row < p.N_q) {
     const float mu = (m_fin == -INFINITY) ? 0.0f : m_fin;
+    const float shift = FP8 ? static_cast<float>(kPShift8) : 0.0f;
     p.lse[static_cast<size_t>(bh) * p.N_q + row] =
-        (l_row > 0.0f) ? (mu + lg2(l_row)) * 0.69314718055994531f : -INFINITY;
+        (l_row > 0.0f) ? (mu + lg2(l_row) - shift) * 0.69314718055994531f : -INFINITY;
   }
   return true;
 }
 
-template <int D, bool BF16, int KS, int VS>
+template <int D, bool BF16, int KS, int VS, bool FP8 = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
-  using L = FwdLayout<D, KS, VS>;
+  using L = FwdLayout<D, KS, VS, FP8>;
+  // 128-byte swizzled column chunks of a Q/K tile row: 64 16-bit or 128 8-bit elements
+  constexpr int kChunks = FP8 ? 1 : D / 64;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -363,7 +380,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const FwdItem nx = decode_item(x, p);
           if (nx.n_tiles > 0) {
 #pragma unroll
-            for (int sub = 0; sub < D / 64; ++sub) tma_prefetch_l2_3d(&tm_q, sub * 64, nx.q0, nx.bh);
+            for (int sub = 0; sub < kChunks; ++sub) tma_prefetch_l2_3d(&tm_q, sub * 64, nx.q0, nx.bh);
           }
         } else {
           next_id = -1;
@@ -403,7 +420,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           mbar_arrive_expect_tx(BAR_K(s), L::kKVBytes);
 #pragma unroll
-          for (int sub = 0; sub < D / 64; ++sub)
+          for (int sub = 0; sub < kChunks; ++sub)
             tma_load_3d(sK + s * L::kKVBytes + sub * kSubTile, &tm_k, BAR_K(s), sub * 64,
                         kt * kBlockN, it.kv_plane);
           ++T;
@@ -414,7 +431,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             mbar_arrive_expect_tx(FBAR(kBarQFull), L::kQBytes);
 #pragma unroll
-            for (int sub = 0; sub < D / 64; ++sub)
+            for (int sub = 0; sub < kChunks; ++sub)
               tma_load_3d(sQ + sub * kSubTile, &tm_q, FBAR(kBarQFull), sub * 64, it.q0, it.bh);
             ++kq;
           }
@@ -458,10 +475,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(BAR_V(s), L::kKVBytes);
+          if constexpr (FP8) {
+            // V^T tile: d rows of 128 keys (the K-major B operand of the 8-bit P V product)
+            tma_load_3d(sV + s * L::kKVBytes, &tm_v, BAR_V(s), kt * kBlockN, 0, it.kv_plane);
+          } else {
 #pragma unroll
-          for (int sub = 0; sub < D / 64; ++sub)
-            tma_load_3d(sV + s * L::kKVBytes + sub * kSubTile, &tm_v, BAR_V(s), sub * 64,
-                        kt * kBlockN, it.kv_plane);
+            for (int sub = 0; sub < D / 64; ++sub)
+              tma_load_3d(sV + s * L::kKVBytes + sub * kSubTile, &tm_v, BAR_V(s), sub * 64,
+                          kt * kBlockN, it.kv_plane);
+          }
           ++T;
         }
       }
@@ -477,8 +499,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // issuer's MMAs.
     if (lane == 0) {
       const bool qk_issuer = (warp == kQkWarp);
-      constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kBlockM, kBlockN, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kBlockM, D, true);
+      // (FP8: kind::f8f6f4 with format code 0 = E4M3 for A and B; V^T is K-major)
+      constexpr uint32_t idesc_qk = make_idesc_f16(BF16 && !FP8, kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_pv = make_idesc_f16(BF16 && !FP8, kBlockM, D, !FP8);
       // S_t = Q K_t^T into S buffer t % 2, once the softmax of tile t - 2 has read that buffer.
       auto issue_qk = [&](int t) -> bool {
         FWD_TRACE(t, 8);
@@ -491,14 +514,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         FWD_TRACE(t, 9);
         tc_fence_after();
         const uint32_t s_col = tmem + ((t & 1) ? kColS1 : kColS0);
+        if constexpr (FP8) {
+          // 8-bit Q and K, K-major: 32 elements = 32 bytes per MMA in the one 128-byte row
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // Q and K are K-major (d contiguous): 16 elements = 32 bytes per MMA inside the
-          // 128-byte swizzle row; SBO = 1024 B between 8-row groups.
-          const uint32_t off = (kk >> 2) * kSubTile + (kk & 3) * 32;
-          const uint64_t adesc = make_sdesc_sw128(sQ + off, 16, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(sK + s * L::kKVBytes + off, 16, 1024);
-          mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk) {
+            const uint64_t adesc = make_sdesc_sw128(sQ + kk * 32, 16, 1024);
+            const uint64_t bdesc = make_sdesc_sw128(sK + s * L::kKVBytes + kk * 32, 16, 1024);
+            mma_ss_f8(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // Q and K are K-major (d contiguous): 16 elements = 32 bytes per MMA inside the
+            // 128-byte swizzle row; SBO = 1024 B between 8-row groups.
+            const uint32_t off = (kk >> 2) * kSubTile + (kk & 3) * 32;
+            const uint64_t adesc = make_sdesc_sw128(sQ + off, 16, 1024);
+            const uint64_t bdesc = make_sdesc_sw128(sK + s * L::kKVBytes + off, 16, 1024);
+            mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(FBAR(kBarS + (t & 1)));
         mma_commit(BAR_KE(s));  // K slot free
@@ -516,14 +549,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         FWD_TRACE(t, 13);
         tc_fence_after();
         const uint32_t p_col = tmem + ((t & 1) ? PCols<D>::kP1 : PCols<D>::kP0);
+        if constexpr (FP8) {
+          // P: E4M3 codes, four per tensor-memory column; V^T rows (d) of 128 keys, K-major:
+          // 32 keys = 32 bytes per MMA in the 128-byte row
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          // V is [keys, d] with d contiguous: the B operand is MN-major.  16 keys per MMA
-          // (two 8-row groups, SBO = 1024 B apart); the two 64-column halves of d are
-          // separate swizzled sub-tiles (LBO = one sub-tile).
-          const uint64_t bdesc = make_sdesc_sw128(sV + s * L::kKVBytes + kk * 16 * 128,
-                                                  kSubTile, 1024);
-          mma_ts(tmem + kColO, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlockN / 32; ++kk) {
+            const uint64_t bdesc = make_sdesc_sw128(sV + s * L::kKVBytes + kk * 32, 16, 1024);
+            mma_ts_f8(tmem + kColO, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            // V is [keys, d] with d contiguous: the B operand is MN-major.  16 keys per MMA
+            // (two 8-row groups, SBO = 1024 B apart); the two 64-column halves of d are
+            // separate swizzled sub-tiles (LBO = one sub-tile).
+            const uint64_t bdesc = make_sdesc_sw128(sV + s * L::kKVBytes + kk * 16 * 128,
+                                                    kSubTile, 1024);
+            mma_ts(tmem + kColO, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(FBAR(kBarO + (t & 1)));
         mma_commit(BAR_VE(s));  // V slot free
@@ -731,11 +774,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_read = mrow[r];
         }
         const float m_prev = (i > 0) ? m_read : -INFINITY;
-        // The maximum moves only when it rises by more than 2^8 (also for the first finite one).
+        // Score scale of this tile: scale * log2(e), times the E4M3 block scales for FP8.
+        float tsc = sl2;
+        if constexpr (FP8)
+          tsc = sl2 * p.q_scale[static_cast<size_t>(it.bh) * p.n_qtiles + it.q0 / kBlockM] *
+                p.k_scale[static_cast<size_t>(it.kv_plane) * p.n_kvtiles + j];
+        // The maximum moves only when it rises by more than 2^8 (also for the first finite one);
+        // FP8: by more than 2^1.
         float m_j = m_prev;
         float alpha = 1.0f;  // rescale of the accumulator O for this tile
-        const float m_new = fmaxf(m_prev, tile_max * sl2);
-        if (m_new - m_prev > kRescaleThreshold) {
+        const float m_new = fmaxf(m_prev, tile_max * tsc);
+        if (m_new - m_prev > (FP8 ? kRescaleThreshold8 : kRescaleThreshold)) {
           alpha = ex2(m_prev - m_new);
           m_j = m_new;
         }
@@ -745,20 +794,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           l = (m_own == -INFINITY) ? 0.0f : l * ex2(m_own - m_j);
           m_own = m_j;
         }
-        const float neg_mu = (m_j == -INFINITY) ? 0.0f : -m_j;
+        const float neg_mu = ((m_j == -INFINITY) ? 0.0f : -m_j) + (FP8 ? kPShift8 : 0);
         // p = 2^(x * scale * log2(e) - m): one packed FMA per pair of scores, MUFU ex2, a packed
-        // add into four pair-accumulators for the row sum, and the 16-bit pack for P.
+        // add into four pair-accumulators for the row sum, and the 16-bit pack for P (FP8:
+        // 2^7 p, four E4M3 codes per word).
         float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[2][32];
 #pragma unroll
-        for (int c = 0; c < kBlockN; c += 2) {
-          float a0, a1;
-          fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_mu, neg_mu);
-          const float p0 = ex2(a0);
-          const float p1 = ex2(a1);
+        for (int c = 0; c < kBlockN; c += 4) {
+          float a0, a1, a2, a3;
+          fma2(a0, a1, x[c], x[c + 1], tsc, tsc, neg_mu, neg_mu);
+          fma2(a2, a3, x[c + 2], x[c + 3], tsc, tsc, neg_mu, neg_mu);
+          const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
           const int k2 = ((c >> 1) & 3) * 2;
           add2(ps[k2], ps[k2 + 1], p0, p1);
-          pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
+          add2(ps[k2 + 2], ps[k2 + 3], p2, p3);
+          if constexpr (FP8) {
+            pk[0][c >> 2] = pack4_e4m3(p0, p1, p2, p3);
+          } else {
+            pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
+            pk[c >> 6][((c >> 1) & 31) + 1] = pack2<BF16>(p2, p3);
+          }
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         // Tile t + 2 is this warpgroup's next one, in this item or the next.
@@ -774,7 +830,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         if (tracer) FWD_TRACE(t, 4);
         tmem_st32(row_tmem + p_col, pk[0]);
-        tmem_st32(row_tmem + p_col + 32, pk[1]);
+        if constexpr (!FP8) tmem_st32(row_tmem + p_col + 32, pk[1]);
         // Both cases below need P V_{t-1} finished: P V_t waits for this tile's P and P V_{t+1}
         // comes after it, so nothing else touches the accumulator meanwhile.
         const bool rescale = i > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
@@ -800,7 +856,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // The first tile after the owed item's last one: its accumulator is read out before
           // this tile's P is released to P V_t, which overwrites it.
           if (tracer) FWD_TRACE(ep_state[3], 6);
-          if (!run_epilogue<D, BF16>(row_tmem + kColO, m_read, ep_l, ep_m, ep_state[0],
+          if (!run_epilogue<D, BF16, FP8>(row_tmem + kColO, m_read, ep_l, ep_m, ep_state[0],
                                      ep_state[1], ep_state[2], r,
                                      fbars, lpart, gbase + L::kOst, p, abort_flag)) {
             ok = false;
@@ -857,7 +913,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       done = done && warp_wait(FBAR(kBarO + (t_e & 1)), (t_e >> 1) & 1, abort_flag, p.status);
       if (done && warp_wait(FBAR(kBarM + (t_e & 1)), (t_e >> 1) & 1, abort_flag, p.status)) {
         tc_fence_after();
-        run_epilogue<D, BF16>(row_tmem + kColO, mrow[r], ep_l, ep_m, ep_state[0], ep_state[1],
+        run_epilogue<D, BF16, FP8>(row_tmem + kColO, mrow[r], ep_l, ep_m, ep_state[0], ep_state[1],
                               ep_state[2], r, fbars,
                               lpart, gbase + L::kOst, p, abort_flag);
       }
@@ -881,18 +937,28 @@ __global__ void attn_empty_rows_kernel(uint16_t* o, float* lse, size_t rows, int
   if (i < rows) lse[i] = -INFINITY;
 }
 
-template <int D, bool BF16, int KS, int VS>
+template <int D, bool BF16, int KS, int VS, bool FP8 = false>
 static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
-  using L = FwdLayout<D, KS, VS>;
+  using L = FwdLayout<D, KS, VS, FP8>;
   CUtensorMap tq, tk, tv, to;
   const uint64_t bhq = static_cast<uint64_t>(a.B) * a.Hq;
   const uint64_t bhk = static_cast<uint64_t>(a.B) * a.Hkv;
   const uint64_t rq = static_cast<uint64_t>(D) * 2, rk = rq;
-  if (!make_tmap_3d(&tq, a.q, BF16, D, a.N_q, bhq, rq, rq * a.N_q, 64, kBlockM, 1) ||
-      !make_tmap_3d(&tk, a.k, BF16, D, a.N_kv, bhk, rk, rk * a.N_kv, 64, kBlockN, 1) ||
-      !make_tmap_3d(&tv, a.v, BF16, D, a.N_kv, bhk, rk, rk * a.N_kv, 64, kBlockN, 1) ||
-      !make_tmap_3d(&to, a.o, BF16, D, a.N_q, bhq, rq, rq * a.N_q, 64, kBlockM, 1))
-    return -5;
+  if constexpr (FP8) {
+    // E4M3 codes: Q and K rows of d bytes (one 128-byte swizzle chunk at d = 128); V^T rows of
+    // nkvp keys, loaded as d x 128-key tiles
+    if (!make_tmap_3d_u8(&tq, a.q8, D, a.N_q, bhq, D, static_cast<uint64_t>(D) * a.N_q, D, kBlockM, 1) ||
+        !make_tmap_3d_u8(&tk, a.k8, D, a.N_kv, bhk, D, static_cast<uint64_t>(D) * a.N_kv, D, kBlockN, 1) ||
+        !make_tmap_3d_u8(&tv, a.vt8, a.nkvp, D, bhk, a.nkvp, static_cast<uint64_t>(a.nkvp) * D,
+                         kBlockN, D, 1))
+      return -5;
+  } else {
+    if (!make_tmap_3d(&tq, a.q, BF16, D, a.N_q, bhq, rq, rq * a.N_q, 64, kBlockM, 1) ||
+        !make_tmap_3d(&tk, a.k, BF16, D, a.N_kv, bhk, rk, rk * a.N_kv, 64, kBlockN, 1) ||
+        !make_tmap_3d(&tv, a.v, BF16, D, a.N_kv, bhk, rk, rk * a.N_kv, 64, kBlockN, 1))
+      return -5;
+  }
+  if (!make_tmap_3d(&to, a.o, BF16, D, a.N_q, bhq, rq, rq * a.N_q, 64, kBlockM, 1)) return -5;
   FwdParams p;
   p.o = a.o;
   p.lse = a.lse;
@@ -907,6 +973,9 @@ static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
   p.window = a.window;
   p.n_kvtiles = (a.N_kv + kBlockN - 1) / kBlockN;
   p.block_mask = a.block_mask;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   p.BH = static_cast<int>(bhq);
   {
     // Query heads whose K/V planes fill about half of L2, a multiple of the heads sharing one
@@ -919,7 +988,7 @@ static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
         v = 64 << 20;
       l2_bytes = v;
     }
-    const uint64_t plane_bytes = 2ull * a.N_kv * D * 2;
+    const uint64_t plane_bytes = 2ull * a.N_kv * D * L::kElem;
     uint64_t planes = (static_cast<uint64_t>(l2_bytes) / 2) / plane_bytes;
     if (planes < 1) planes = 1;
     uint64_t heads = planes * static_cast<uint64_t>(a.Hq / a.Hkv);
@@ -928,7 +997,7 @@ static int launch_fwd_variant(const FwdArgs& a, cudaStream_t stream) {
   }
   p.sl2 = a.scale * 1.4426950408889634f;
   if (!p.status) return -5;
-  auto kern = attn_fwd_kernel<D, BF16, KS, VS>;
+  auto kern = attn_fwd_kernel<D, BF16, KS, VS, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
       cudaSuccess)
     return -5;
@@ -946,6 +1015,12 @@ extern "C" int attn_fwd_trace_copy(void* dst) {
 }
 namespace attn {
 #endif
+
+int launch_attn_fwd_fp8_kernel(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d != 128) return -2;
+  return a.bf16 ? launch_fwd_variant<128, true, 4, 4, true>(a, stream)
+                : launch_fwd_variant<128, false, 4, 4, true>(a, stream);
+}
 
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (a.B == 0 || a.N_q == 0) return 0;

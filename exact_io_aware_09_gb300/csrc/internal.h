@@ -14,6 +14,11 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, 
                   uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                   uint32_t box1, uint32_t box2);
 
+// The same over a contiguous 8-bit tensor (E4M3 codes).
+bool make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                     uint32_t box1, uint32_t box2);
+
 // Device address of the status word of the current device (nullptr on failure).
 int* device_status_ptr();
 
@@ -91,6 +96,15 @@ struct FwdArgs {
   bool bf16;
   int window;                 // sliding window (keys behind the diagonal); -1 = none
   const uint8_t* block_mask;  // [ceil(N_q/128)][ceil(N_kv/128)] tiles to compute; null = all
+  // FP8 operands (set by the FP8 entry point after its preparation): E4M3 codes of the rotated
+  // Q [B*Hq, N_q, d] and K [B*Hkv, N_kv, d], of V transposed [B*Hkv, d, nkvp], and their scales
+  const void* q8 = nullptr;
+  const void* k8 = nullptr;
+  const void* vt8 = nullptr;
+  const float* q_scale = nullptr;
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
+  int nkvp = 0;
 };
 
 struct DecodeArgs {
@@ -131,6 +145,12 @@ struct BwdArgs {
 
 // Launchers (return an attn_status_t value).
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+int launch_attn_fwd_fp8_kernel(const FwdArgs& a, cudaStream_t stream);
+// FP8 forward: prepares the rotated, quantised operands in `workspace` (layout from
+// fp8_workspace_layout: Q8, K8, V^T8, Q scales, K scales, V scales, V amax) and runs the kernel.
+int launch_attn_fwd_fp8(const FwdArgs& a, const int8_t* signs, void* workspace,
+                        cudaStream_t stream);
+size_t fp8_workspace_layout(int B, int Hq, int Hkv, int N_q, int N_kv, int d, size_t off[7]);
 int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int N_q);

@@ -119,6 +119,37 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
              size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8 -- prefill attention on FP8 tensor cores with incoherent processing ("FlashAttention
+ * Explained", section "FP8 Attention and Incoherent Processing": Q and K multiplied by the same
+ * random orthogonal matrix M -- a Hadamard transform with random sign flips -- before
+ * quantisation, so (Q M)(K M)^T = Q K^T while outlier channels spread over all channels;
+ * E4M3 operands with per-block scaling factors).  An approximation of attn_fwd: it changes the
+ * numerics and needs an accuracy gate, as the pages say.
+ *
+ * Arguments as attn_fwd (d must be 128), plus
+ *   signs      device int8 [d] of +-1, the random sign flips of M (caller-drawn); null: no
+ *              rotation (plain block-scaled FP8)
+ *   workspace  device, >= attn_fwd_fp8_workspace_bytes(...) bytes, caller-owned; receives the
+ *              E4M3 operands and their scales (layout: attn_fwd_fp8_workspace_offsets)
+ * Q and K rows are rotated (fp32, fast Walsh-Hadamard butterflies) and quantised with one scale
+ * per 128-row tile (amax / 448); V is quantised with one scale per (batch, key/value head) and
+ * stored transposed; P enters the P V product as E4M3.  O is written in `dtype`, L in fp32 as
+ * attn_fwd.  Returns ATTN_OK or a negative attn_status_t.
+ */
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int N_q, int N_kv, int d);
+
+/* attn_fwd_fp8_workspace_offsets -- byte offsets in that workspace of: Q codes [B*Hq, N_q, d],
+ * K codes [B*Hkv, N_kv, d], V^T codes [B*Hkv, d, nkvp] (nkvp = N_kv rounded up to 128), Q scales
+ * [B*Hq, ceil(N_q/128)], K scales [B*Hkv, ceil(N_kv/128)], V scales [B*Hkv] (fp32), scratch. */
+int attn_fwd_fp8_workspace_offsets(int B, int Hq, int Hkv, int N_q, int N_kv, int d,
+                                   size_t *offsets /* [7] */);
+
+int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                 int Hkv, int N_q, int N_kv, int d, int causal, float scale, const int8_t *signs,
+                 void *workspace, size_t workspace_bytes, attn_stream_t stream,
+                 attn_dtype_t dtype);
+
+/*
  * attn_fwd_window -- prefill attention with a sliding window, the mask that changes the
  * operator ("FlashAttention Explained", FlexAttention section, sliding_causal: key kv is visible
  * to query q iff q >= kv and q - kv <= W; "FlashAttention, annotated", section on causal masks

@@ -63,6 +63,33 @@ def scale_bits_pow2(bits: np.ndarray, dtype: str, k: int) -> np.ndarray:
     return y.view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def bits_to_float32(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Values of stored fp16 / bf16 bits as float32 (exact)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == F16:
+        return bits.view(np.float16).astype(np.float32)
+    if dtype == BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def random_signs(d: int, seed: int) -> np.ndarray:
+    """int8 [d] of independent, equally likely +-1 (the sign flips of a randomised Hadamard
+    rotation)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return np.where(g.random(d) < 0.5, -1, 1).astype(np.int8)
+
+
+def with_outliers(bits: np.ndarray, dtype: str, seed: int, frac: float = 1e-3,
+                  pow2: int = 4) -> np.ndarray:
+    """A fraction ``frac`` of the entries, chosen at random, multiplied by 2**pow2 exactly
+    (large outliers among N(0,1) activations)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    pick = g.random(bits.shape) < frac
+    big = scale_bits_pow2(bits, dtype, pow2)
+    return np.where(pick, big, bits).astype(np.uint16)
+
+
 def torch_dtype(dtype: str):
     torch = _torch()
     return torch.float16 if dtype == F16 else torch.bfloat16

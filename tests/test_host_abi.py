@@ -119,6 +119,22 @@ def test_workspace_bytes(attn):
     assert attn.attn_decode_workspace_bytes(1, 1, 1, 512, 64) >= 66 * 4
 
 
+def test_fp8_workspace_layout(attn):
+    B, Hq, Hkv, Nq, Nkv, d = 2, 8, 2, 300, 1000, 128
+    off = attn.attn_fwd_fp8_workspace_offsets(B, Hq, Hkv, Nq, Nkv, d)
+    total = attn.attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, d)
+    nqt, nkt = -(-Nq // 128), -(-Nkv // 128)
+    sizes = [B * Hq * Nq * d, B * Hkv * Nkv * d, B * Hkv * d * nkt * 128, B * Hq * nqt * 4,
+             B * Hkv * nkt * 4, B * Hkv * 4, B * Hkv * 4]
+    assert off[0] == 0
+    for i in range(7):
+        assert off[i] % 256 == 0
+        end = off[i] + sizes[i]
+        assert end <= (off[i + 1] if i < 6 else total)
+    assert total - (off[6] + sizes[6]) < 256
+    assert attn.attn_fwd_fp8_workspace_bytes(0, Hq, Hkv, Nq, Nkv, d) == 0
+
+
 def test_bad_arguments_are_refused_before_launch(attn):
     L = attn.lib
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails its checks
@@ -154,6 +170,18 @@ def test_bad_arguments_are_refused_before_launch(attn):
     assert dec(cu=ctypes.c_void_p((1 << 20) + 2)) == -3
     if no_device:
         assert dec() == -7
+    def fp8(d=128, ws_bytes=1 << 30, ws=fake, signs=nul, B=1, nkv=300):
+        return L.attn_fwd_fp8(fake, fake, fake, fake, fake, B, 4, 2, 200, nkv, d, 1, s, signs, ws,
+                              ws_bytes, nul, 1)
+
+    assert fp8(d=64) == -2
+    assert fp8(ws_bytes=1024) == -4
+    assert fp8(ws=nul) == -4
+    assert fp8(ws=odd) == -3
+    assert fp8(B=0) == 0
+    if no_device:
+        assert fp8() == -7
+        assert fp8(signs=fake) == -7
     assert L.attn_selftest_timeout(0, nul) == -1
     assert L.attn_selftest_timeout(2_000_000, nul) == -1
 
