@@ -22,17 +22,51 @@ namespace attn {
 
 namespace {
 
-constexpr int kT = 128;  // rows of a tile
+constexpr int kT = 128;        // rows of a tile
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
 
+// Four consecutive 16-bit values (8 bytes) as floats.
 template <bool BF16>
-__device__ __forceinline__ float load_half(const uint16_t* p) {
-  const uint32_t h = *p;
-  if constexpr (BF16) {
-    return __uint_as_float(h << 16);
-  } else {
-    float f;
-    asm("{\n\t.reg .f16 t;\n\tmov.b16 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "h"(static_cast<uint16_t>(h)));
-    return f;
+__device__ __forceinline__ void load4(const uint16_t* p, float v[4]) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  const uint32_t h[2] = {w.x, w.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if constexpr (BF16) {
+      v[2 * i] = __uint_as_float(h[i] << 16);
+      v[2 * i + 1] = __uint_as_float(h[i] & 0xffff0000u);
+    } else {
+      float lo, hi;
+      asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+          "cvt.f32.f16 %1, b;\n\t}"
+          : "=f"(lo), "=f"(hi)
+          : "r"(h[i]));
+      v[2 * i] = lo;
+      v[2 * i + 1] = hi;
+    }
+  }
+}
+
+// Eight consecutive 16-bit values (16 bytes) as floats.
+template <bool BF16>
+__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16) {
+      v[2 * i] = __uint_as_float(h[i] << 16);
+      v[2 * i + 1] = __uint_as_float(h[i] & 0xffff0000u);
+    } else {
+      float lo, hi;
+      asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+          "cvt.f32.f16 %1, b;\n\t}"
+          : "=f"(lo), "=f"(hi)
+          : "r"(h[i]));
+      v[2 * i] = lo;
+      v[2 * i + 1] = hi;
+    }
   }
 }
 
@@ -46,109 +80,166 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
+__device__ __forceinline__ float scale_of(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
 }  // namespace
 
-// One block per (plane, 128-row tile), thread = row: rotate (optional), tile amax, quantise.
+// One block per (plane, 128-row tile) of Q or of K (blocks [0, q_blocks) take Q): rotate
+// (optional), tile amax, quantise.  A warp takes one row at a time, lane l holding channels
+// 4l .. 4l+3, so that loads (8 bytes a lane) and code stores (4 bytes a lane) are coalesced.
+// Butterfly stages h = 1, 2 are inside a lane; stage h = 4m pairs lane l with lane l ^ m: the
+// lane without bit m keeps a + b, the other b' = a - b, the same fp32 operations in the same
+// order as the plain loop over j.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kT)
-    fp8_rotate_quantize_kernel(const uint16_t* x, const int8_t* signs, float inv_sqrt_d,
-                               uint8_t* codes, float* scales, int N, int n_tiles) {
-  __shared__ float red[kT / 32];
-  const int plane = blockIdx.x / n_tiles;
-  const int tile = blockIdx.x % n_tiles;
-  const int row = tile * kT + threadIdx.x;
-  const bool live = row < N;
-  float v[D];
-  const uint16_t* src = x + (static_cast<size_t>(plane) * N + (live ? row : 0)) * D;
-#pragma unroll
-  for (int c = 0; c < D; ++c) v[c] = live ? load_half<BF16>(src + c) : 0.0f;
+__global__ void __launch_bounds__(kPrepThreads)
+    fp8_rotate_quantize_kernel(const uint16_t* xq, const uint16_t* xk, const int8_t* signs,
+                               float inv_sqrt_d, uint8_t* cq, uint8_t* ck, float* sq, float* sk,
+                               int Nq, int Nk, int nqt, int nkt, int q_blocks) {
+  static_assert(D == 128, "one 4-channel slice per lane");
+  constexpr int kRows = kT / kPrepWarps;  // rows per warp
+  __shared__ float red[kPrepWarps];
+  const bool is_q = static_cast<int>(blockIdx.x) < q_blocks;
+  const int b = is_q ? blockIdx.x : blockIdx.x - q_blocks;
+  const int n_tiles = is_q ? nqt : nkt;
+  const int N = is_q ? Nq : Nk;
+  const uint16_t* x = is_q ? xq : xk;
+  uint8_t* codes = is_q ? cq : ck;
+  const int plane = b / n_tiles, tile = b % n_tiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float sg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
   if (signs) {
 #pragma unroll
-    for (int c = 0; c < D; ++c) v[c] = signs[c] < 0 ? -v[c] : v[c];
+    for (int e = 0; e < 4; ++e) sg[e] = signs[4 * lane + e] < 0 ? -1.0f : 1.0f;
+  }
+  float v[kRows][4];
 #pragma unroll
-    for (int h = 1; h < D; h <<= 1)
+  for (int i = 0; i < kRows; ++i) {
+    const int row = tile * kT + warp + i * kPrepWarps;
+    if (row < N) {
+      load4<BF16>(x + (static_cast<size_t>(plane) * N + row) * D + 4 * lane, v[i]);
+    } else {
 #pragma unroll
-      for (int j = 0; j < D; ++j)
-        if ((j & h) == 0) {
-          const float a = v[j], b = v[j + h];
-          v[j] = a + b;
-          v[j + h] = a - b;
-        }
-#pragma unroll
-    for (int c = 0; c < D; ++c) v[c] = v[c] * inv_sqrt_d;
+      for (int e = 0; e < 4; ++e) v[i][e] = 0.0f;
+    }
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int c = 0; c < D; ++c) amax = fmaxf(amax, fabsf(v[c]));
-  amax = block_max(amax, red);
-  const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  if (threadIdx.x == 0) scales[blockIdx.x] = scale;
-  if (!live) return;
-  uint4* dst = reinterpret_cast<uint4*>(codes + (static_cast<size_t>(plane) * N + row) * D);
+  for (int i = 0; i < kRows; ++i) {
+    if (signs) {
 #pragma unroll
-  for (int c = 0; c < D; c += 16) {
-    uint4 w;
-    w.x = pack4_e4m3(__fdiv_rn(v[c + 0], scale), __fdiv_rn(v[c + 1], scale),
-                     __fdiv_rn(v[c + 2], scale), __fdiv_rn(v[c + 3], scale));
-    w.y = pack4_e4m3(__fdiv_rn(v[c + 4], scale), __fdiv_rn(v[c + 5], scale),
-                     __fdiv_rn(v[c + 6], scale), __fdiv_rn(v[c + 7], scale));
-    w.z = pack4_e4m3(__fdiv_rn(v[c + 8], scale), __fdiv_rn(v[c + 9], scale),
-                     __fdiv_rn(v[c + 10], scale), __fdiv_rn(v[c + 11], scale));
-    w.w = pack4_e4m3(__fdiv_rn(v[c + 12], scale), __fdiv_rn(v[c + 13], scale),
-                     __fdiv_rn(v[c + 14], scale), __fdiv_rn(v[c + 15], scale));
-    dst[c / 16] = w;
+      for (int e = 0; e < 4; ++e) v[i][e] = sg[e] < 0.0f ? -v[i][e] : v[i][e];
+      // h = 1: (0, 1), (2, 3); h = 2: (0, 2), (1, 3)
+      float a = v[i][0], c = v[i][1];
+      v[i][0] = a + c;
+      v[i][1] = a - c;
+      a = v[i][2];
+      c = v[i][3];
+      v[i][2] = a + c;
+      v[i][3] = a - c;
+      a = v[i][0];
+      c = v[i][2];
+      v[i][0] = a + c;
+      v[i][2] = a - c;
+      a = v[i][1];
+      c = v[i][3];
+      v[i][1] = a + c;
+      v[i][3] = a - c;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, v[i][e], m);
+          v[i][e] = upper ? other - v[i][e] : v[i][e] + other;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[i][e] = v[i][e] * inv_sqrt_d;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+  }
+  const float scale = scale_of(block_max(amax, red));
+  if (threadIdx.x == 0) (is_q ? sq : sk)[b] = scale;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int row = tile * kT + warp + i * kPrepWarps;
+    if (row < N)
+      *reinterpret_cast<uint32_t*>(codes + (static_cast<size_t>(plane) * N + row) * D + 4 * lane) =
+          pack4_e4m3(__fdiv_rn(v[i][0], scale), __fdiv_rn(v[i][1], scale),
+                     __fdiv_rn(v[i][2], scale), __fdiv_rn(v[i][3], scale));
   }
 }
 
-// Per-plane amax of V (non-negative floats order as their bit patterns).
+// Per-plane amax of V over 128-row tiles, 16-byte loads (non-negative floats order as their bit
+// patterns, so an integer atomicMax takes the maximum).
 template <int D, bool BF16>
-__global__ void fp8_plane_amax_kernel(const uint16_t* x, unsigned* amax_bits, int N, int n_tiles) {
-  __shared__ float red[kT / 32];
-  const int plane = blockIdx.x / n_tiles;
-  const int row = (blockIdx.x % n_tiles) * kT + threadIdx.x;
+__global__ void __launch_bounds__(kPrepThreads)
+    fp8_plane_amax_kernel(const uint16_t* x, unsigned* amax_bits, int N, int n_tiles) {
+  __shared__ float red[kPrepWarps];
+  const int plane = blockIdx.x / n_tiles, tile = blockIdx.x % n_tiles;
+  const int rows = min(kT, N - tile * kT);
+  const uint16_t* src = x + (static_cast<size_t>(plane) * N + static_cast<size_t>(tile) * kT) * D;
   float m = 0.0f;
-  if (row < N) {
-    const uint16_t* src = x + (static_cast<size_t>(plane) * N + row) * D;
-#pragma unroll 8
-    for (int c = 0; c < D; ++c) m = fmaxf(m, fabsf(load_half<BF16>(src + c)));
+  for (int c = threadIdx.x; c < rows * (D / 8); c += kPrepThreads) {
+    float v[8];
+    load8<BF16>(src + static_cast<size_t>(c) * 8, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) atomicMax(amax_bits + plane, __float_as_uint(m));
 }
 
-// V -> E4M3 codes transposed to [plane, d, nkvp]; one block per (plane, 128-key tile), thread =
-// key; keys past N get code 0.  The block's 128 keys x d codes pass through shared memory so
-// that each output row (one channel, 128 keys) is written with 16-byte stores.
+// V -> E4M3 codes transposed to [plane, d, nkvp]; one block per (plane, 128-key tile); keys past
+// N get code 0.  A thread converts four keys x eight channels (four 16-byte loads, sixteen lanes
+// covering a row), regroups the codes into one 4-key word per channel and stores the words into
+// a shared [d][128 + 4]-byte tile; the tile's rows then go out as 128-byte coalesced rows.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kT)
+__global__ void __launch_bounds__(kPrepThreads)
     fp8_v_transpose_kernel(const uint16_t* x, const unsigned* amax_bits, float* scales,
                            uint8_t* vt, int N, int n_tiles, int nkvp) {
-  __shared__ __align__(16) uint8_t tile[D][kT];
-  const int plane = blockIdx.x / n_tiles;
-  const int kt = blockIdx.x % n_tiles;
-  const int key = kt * kT + threadIdx.x;
-  const float amax = __uint_as_float(amax_bits[plane]);
-  const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  constexpr int kPitch = kT + 4;  // bytes per channel row in shared memory
+  __shared__ __align__(16) uint8_t tile[D * kPitch];
+  const int plane = blockIdx.x / n_tiles, kt = blockIdx.x % n_tiles;
+  const float scale = scale_of(__uint_as_float(amax_bits[plane]));
   if (kt == 0 && threadIdx.x == 0) scales[plane] = scale;
-  const uint16_t* src = x + (static_cast<size_t>(plane) * N + (key < N ? key : 0)) * D;
-#pragma unroll 4
-  for (int c = 0; c < D; c += 4) {
-    uint32_t w = 0;
-    if (key < N)
-      w = pack4_e4m3(__fdiv_rn(load_half<BF16>(src + c), scale),
-                     __fdiv_rn(load_half<BF16>(src + c + 1), scale),
-                     __fdiv_rn(load_half<BF16>(src + c + 2), scale),
-                     __fdiv_rn(load_half<BF16>(src + c + 3), scale));
-    tile[c][threadIdx.x] = w & 0xff;
-    tile[c + 1][threadIdx.x] = (w >> 8) & 0xff;
-    tile[c + 2][threadIdx.x] = (w >> 16) & 0xff;
-    tile[c + 3][threadIdx.x] = w >> 24;
+  const uint16_t* src = x + static_cast<size_t>(plane) * N * D;
+  constexpr int kChunks = D / 8;                 // 8-channel chunks of a row
+  constexpr int kUnits = (kT / 4) * kChunks;     // (key quad, chunk) pairs
+  for (int u = threadIdx.x; u < kUnits; u += kPrepThreads) {
+    const int chunk = u % kChunks, quad = u / kChunks;
+    uint32_t w[4][2];  // codes of key kq*4 + r, channels 8 chunk .. +7
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int key = kt * kT + quad * 4 + r;
+      if (key < N) {
+        float v[8];
+        load8<BF16>(src + static_cast<size_t>(key) * D + chunk * 8, v);
+        w[r][0] = pack4_e4m3(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale),
+                             __fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale));
+        w[r][1] = pack4_e4m3(__fdiv_rn(v[4], scale), __fdiv_rn(v[5], scale),
+                             __fdiv_rn(v[6], scale), __fdiv_rn(v[7], scale));
+      } else {
+        w[r][0] = w[r][1] = 0u;
+      }
+    }
+    // channel e of the chunk: byte e % 4 of word e / 4 of each key -> one word of four keys
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int h = e >> 2, sh = (e & 3) * 8;
+      const uint32_t word = ((w[0][h] >> sh) & 0xffu) | (((w[1][h] >> sh) & 0xffu) << 8) |
+                            (((w[2][h] >> sh) & 0xffu) << 16) | (((w[3][h] >> sh) & 0xffu) << 24);
+      *reinterpret_cast<uint32_t*>(tile + (chunk * 8 + e) * kPitch + quad * 4) = word;
+    }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < D * (kT / 16); i += kT) {
-    const int c = i / (kT / 16), part = i % (kT / 16);
-    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(plane) * D + c) * nkvp + kt * kT + part * 16) =
-        *reinterpret_cast<const uint4*>(&tile[c][part * 16]);
+  for (int u = threadIdx.x; u < D * (kT / 4); u += kPrepThreads) {
+    const int c = u / (kT / 4), word = u % (kT / 4);
+    *reinterpret_cast<uint32_t*>(vt + (static_cast<size_t>(plane) * D + c) * nkvp + kt * kT +
+                                 word * 4) = *reinterpret_cast<const uint32_t*>(tile + c * kPitch + word * 4);
   }
 }
 
@@ -197,17 +288,16 @@ int launch_attn_fwd_fp8(const FwdArgs& a, const int8_t* signs, void* workspace,
   if (cudaMemsetAsync(amax, 0, static_cast<size_t>(pk) * 4, stream) != cudaSuccess) return -5;
   auto run = [&](auto bf16_tag) -> int {
     constexpr bool BF = decltype(bf16_tag)::value;
-    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt, kT, 0, stream>>>(
-        static_cast<const uint16_t*>(a.q), signs, inv_sqrt_d, static_cast<uint8_t*>(const_cast<void*>(f.q8)),
-        const_cast<float*>(f.q_scale), a.N_q, nqt);
-    fp8_rotate_quantize_kernel<D, BF><<<pk * nkt, kT, 0, stream>>>(
-        static_cast<const uint16_t*>(a.k), signs, inv_sqrt_d, static_cast<uint8_t*>(const_cast<void*>(f.k8)),
-        const_cast<float*>(f.k_scale), a.N_kv, nkt);
-    fp8_plane_amax_kernel<D, BF><<<pk * nkt, kT, 0, stream>>>(static_cast<const uint16_t*>(a.v), amax,
-                                                              a.N_kv, nkt);
-    fp8_v_transpose_kernel<D, BF><<<pk * nkt, kT, 0, stream>>>(
-        static_cast<const uint16_t*>(a.v), amax, const_cast<float*>(f.v_scale),
-        static_cast<uint8_t*>(const_cast<void*>(f.vt8)), a.N_kv, nkt, f.nkvp);
+    const uint16_t* v16 = static_cast<const uint16_t*>(a.v);
+    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kPrepThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), signs, inv_sqrt_d,
+        static_cast<uint8_t*>(const_cast<void*>(f.q8)), static_cast<uint8_t*>(const_cast<void*>(f.k8)),
+        const_cast<float*>(f.q_scale), const_cast<float*>(f.k_scale), a.N_q, a.N_kv, nqt, nkt,
+        pq * nqt);
+    fp8_plane_amax_kernel<D, BF><<<pk * nkt, kPrepThreads, 0, stream>>>(v16, amax, a.N_kv, nkt);
+    fp8_v_transpose_kernel<D, BF><<<pk * nkt, kPrepThreads, 0, stream>>>(
+        v16, amax, const_cast<float*>(f.v_scale), static_cast<uint8_t*>(const_cast<void*>(f.vt8)),
+        a.N_kv, nkt, f.nkvp);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
   };
   const int st = a.bf16 ? run(std::true_type{}) : run(std::false_type{});

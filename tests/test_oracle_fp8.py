@@ -98,3 +98,47 @@ def test_rotation_leaves_unquantised_scores_unchanged():
     o2, l2 = fp8.attention_f64(qr, kr, vx, False, cfg.scale)
     np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-5)
     np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-5)
+
+
+def test_prepare_dequantises_to_the_rotated_inputs():
+    """prepare + dequantized: each value is within half an E4M3 step (times its block's scale)
+    of the rotated Q / K and the unrotated V; the scales are amax / 448 of the right block (128
+    rows of one (batch, head) plane for Q and K, the whole plane for V); planes are (batch,
+    head) in that order."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, Nq, Nkv, d = 2, 4, 2, 200, 150, 64
+    q = rng.standard_normal((B, Hq, Nq, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, Nkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, Nkv, d)).astype(np.float32)
+    q[1, 2, 130, 5] = 40.0   # an outlier in one tile of one plane
+    v[0, 1, 7, 3] = -30.0    # and in one V plane
+    signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    prep = fp8.prepare(q, k, v, signs)
+    qd, kd, vd = fp8.dequantized(prep, B, Hq, Hkv, Nq, Nkv, d)
+    H = np.asarray(__import__("scipy.linalg", fromlist=["hadamard"]).hadamard(d), np.float64)
+    M = H @ np.diag(signs) / np.sqrt(d)          # x -> M x, rows as vectors: x M^T
+    qr = q.astype(np.float64) @ M.T
+    kr = k.astype(np.float64) @ M.T
+    for got, ref, sc, rows in ((qd, qr, prep["sq"], 128), (kd, kr, prep["sk"], 128)):
+        b_, h_, n_, _ = ref.shape
+        for b in range(b_):
+            for h in range(h_):
+                for t in range(-(-n_ // rows)):
+                    blk = ref[b, h, t * rows:(t + 1) * rows]
+                    s = sc[b * h_ + h, t]
+                    assert abs(s - np.abs(blk).max() / 448.0) <= 1e-6 * s
+                    err = np.abs(got[b, h, t * rows:(t + 1) * rows] - blk)
+                    # half a step of E4M3 (2^-4 relative, 2^-10 absolute below 2^-6) plus the
+                    # fp32 rotation's rounding
+                    assert np.all(err <= s * np.maximum(np.abs(blk) / s * 2.0 ** -4, 2.0 ** -10)
+                                  + 1e-5)
+    for b in range(B):
+        for h in range(Hkv):
+            s = prep["sv"][b * Hkv + h]
+            assert s == np.float32(np.abs(v[b, h]).max() / np.float32(448.0))
+            err = np.abs(vd[b, h] - v[b, h])
+            assert np.all(err <= s * np.maximum(np.abs(v[b, h]) / s * 2.0 ** -4, 2.0 ** -10))
+    # the outlier's tile: the rotation spreads 40 over 64 channels (5 each), about twice the
+    # tile's other maxima; unrotated V keeps it whole
+    assert prep["sq"][1 * Hq + 2, 1] > 1.5 * prep["sq"][1 * Hq + 2, 0]
+    assert prep["sv"][0 * Hkv + 1] > 5 * prep["sv"][0 * Hkv + 0]
