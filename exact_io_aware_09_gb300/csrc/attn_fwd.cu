@@ -48,7 +48,7 @@ namespace attn {
 // Optional per-tile timestamps for schedule analysis; compiled in only when ATTN_FWD_TRACE is
 // defined (never in the library build).
 #ifdef ATTN_FWD_TRACE
-__device__ unsigned long long g_fwd_trace[8][80][24];
+__device__ unsigned long long g_fwd_trace[8][80][28];
 #define FWD_TRACE(j, ev)                                                                      \
   do {                                                                                        \
     if (trace_slot >= 0 && (j) < 80) {                                                        \
@@ -119,16 +119,17 @@ enum FwdBar : uint32_t {
   kBarSFree = 4,       // [2] S buffer read by the softmax (128 arrivals)
   kBarP = 6,           // [2] P buffer written, O rescaled (128 arrivals)
   kBarO = 8,           // [2] P V of a tile of that parity finished (MMA commit)
-  kBarM = 10,          // [2] running maximum of a tile of that parity published (128 arrivals)
-  kBarLFull = 12,      // [2] partial row sum handed to the epilogue (128 arrivals), by item parity
-  kBarLEmpty = 14,     // [2] ... and read (128 arrivals)
-  kBarItemFull = 16,   // [2] work-item ring slot written
-  kBarItemEmpty = 18,  // [2] ... and read by every role (kItemReaders arrivals)
-  kBarOStageFull = 20, // O of an item written to the staging buffer (128 arrivals)
-  kBarClc = 21,        // cluster-launch-control answer landed
-  kBarDrain = 22,      // both issuers' MMAs finished (two commits)
-  kBarOStage = 23,     // the TMA store of the previous epilogue has read the O staging buffer
-  kNumFixedBars = 24
+  kBarM = 10,          // [2][4] running maximum of a tile of that parity published, one barrier
+                       // per warp (lane quarter): its 32 rows are all the partner warp needs
+  kBarLFull = 18,      // [2] partial row sum handed to the epilogue (128 arrivals), by item parity
+  kBarLEmpty = 20,     // [2] ... and read (128 arrivals)
+  kBarItemFull = 22,   // [2] work-item ring slot written
+  kBarItemEmpty = 24,  // [2] ... and read by every role (kItemReaders arrivals)
+  kBarOStageFull = 26, // O of an item written to the staging buffer (128 arrivals)
+  kBarClc = 27,        // cluster-launch-control answer landed
+  kBarDrain = 28,      // both issuers' MMAs finished (two commits)
+  kBarOStage = 29,     // the TMA store of the previous epilogue has read the O staging buffer
+  kNumFixedBars = 30
 };
 
 template <int D, int KS, int VS, bool FP8 = false>
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(FBAR(kBarSFree + b), kSoftmaxThreads);
       mbar_init(FBAR(kBarP + b), kSoftmaxThreads);
       mbar_init(FBAR(kBarO + b), 1);
-      mbar_init(FBAR(kBarM + b), kSoftmaxThreads);
+      for (int q = 0; q < 4; ++q) mbar_init(FBAR(kBarM + b * 4 + q), 32);
       mbar_init(FBAR(kBarItemFull + b), 1);
       mbar_init(FBAR(kBarItemEmpty + b), kItemReaders);
       mbar_init(FBAR(kBarLFull + b), kSoftmaxThreads);
@@ -651,7 +652,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // with t % 2 == w (S buffer w, P buffer w); in both, thread r owns query row r and warp % 4
     // is its tensor-memory lane quarter.  The running maximum is the only state carried from
     // tile to tile: the warpgroup of tile t publishes m_t as soon as its row maxima are known
-    // (kBarM), and the other warpgroup, on tile t + 1, waits for it before its exponentials.
+    // (kBarM, one barrier per warp: warp q of one warpgroup and warp q of the other own the same
+    // 32 rows), and the other warpgroup, on tile t + 1, waits for it before its exponentials.
     // Each warpgroup keeps its own partial row sum, rescaled whenever the maximum moves.
     //
     // Epilogue of an item whose last tile is t_e: the warpgroup of t_e hands its partial sum
@@ -775,8 +777,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // item: the previous item's final maximum, which an owed epilogue needs).  The wait also
         // orders this tile's write of mrow after the other warpgroup's read of it.
         float m_read = -INFINITY;
+        if (tracer) FWD_TRACE(t, 24);
         if (t > 0) {
-          if (!warp_wait(FBAR(kBarM + (wg ^ 1)), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
+          if (!warp_wait(FBAR(kBarM + (wg ^ 1) * 4 + quarter), ((t - 1) >> 1) & 1, abort_flag,
+                         p.status)) {
             ok = false;
             break;
           }
@@ -796,7 +800,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_j = m_new;
         }
         mrow[r] = m_j;
-        mbar_arrive(FBAR(kBarM + wg));  // m_t published for tile t + 1
+        mbar_arrive(FBAR(kBarM + wg * 4 + quarter));  // m_t published for tile t + 1
+        if (tracer) FWD_TRACE(t, 25);
         if (m_j != m_own) {
           l = (m_own == -INFINITY) ? 0.0f : l * ex2(m_own - m_j);
           m_own = m_j;
@@ -918,7 +923,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (t_e >= 1)
         done = warp_wait(FBAR(kBarO + ((t_e - 1) & 1)), ((t_e - 1) >> 1) & 1, abort_flag, p.status);
       done = done && warp_wait(FBAR(kBarO + (t_e & 1)), (t_e >> 1) & 1, abort_flag, p.status);
-      if (done && warp_wait(FBAR(kBarM + (t_e & 1)), (t_e >> 1) & 1, abort_flag, p.status)) {
+      if (done && warp_wait(FBAR(kBarM + (t_e & 1) * 4 + quarter), (t_e >> 1) & 1, abort_flag,
+                            p.status)) {
         tc_fence_after();
         run_epilogue<D, BF16, FP8>(row_tmem + kColO, mrow[r], ep_l, ep_m, ep_state[0], ep_state[1],
                               ep_state[2], r, fbars,
