@@ -11,17 +11,24 @@
 //   kernel 0  D and L log2(e) per query row (padded to whole 128-row tiles);
 //   kernel 1  one block per 128-key tile of one (batch, key/value head): loops over the query
 //             tiles of every query head that shares the key/value head and keeps dK and dV in
-//             tensor memory (four MMAs per tile pair: S^T, dP^T, dV += P^T dO, dK += dS^T Q);
+//             tensor memory (four MMAs per step: S^T, dP^T, dV += P^T dO, dK += dS^T Q);
 //   kernel 2  one block per 128-row query tile: loops over the key tiles and keeps dQ in
-//             tensor memory (three MMAs per tile pair: S, dP, dQ += dS K).
+//             tensor memory (three MMAs per step: S, dP, dQ += dS K).
 // S and dP are recomputed in both kernels (seven MMAs per tile pair instead of five): the price
 // of owning every output without atomics.
 //
-// Roles inside a thread block (192 threads): warps 0-3 the elementwise step (thread = one row of
-// the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 4 the TMA producer,
-// warp 5 the tcgen05 issuer (and the tensor-memory allocation).  Both probabilities and dS go
-// back to tensor memory as 16-bit pairs, in place over the fp32 tiles they came from, and feed
-// the next MMAs as their A operand.  Every wait on a barrier is bounded.
+// Both kernels use 128 x 128 x 16 MMAs only (a tcgen05.mma takes about as long at N = 64 as at
+// N = 128, so narrower steps waste the tensor pipe), and two elementwise warpgroups that split
+// each tile's 128 columns.  The elementwise step writes its 16-bit results over the fp32
+// columns it has already read, which frees the dP buffer as soon as it has been read, so that
+// the next tile's dP product overlaps this tile's dS step.
+//
+// Roles inside a thread block (320 threads): warps 0-3 and 4-7 two elementwise warpgroups, one
+// per half of a tile's columns (thread = one row of the tensor-memory tiles: a key in kernel 1,
+// a query in kernel 2), warp 8 the TMA producer, warp 9 the tcgen05 issuer (and the
+// tensor-memory allocation).  Probabilities and dS go back to
+// tensor memory as 16-bit pairs, in place over the fp32 tiles they came from, and feed the next
+// MMAs as their A operand.  Every wait on a barrier is bounded.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,9 +37,9 @@ namespace attn {
 namespace {
 
 constexpr int kBT = 128;            // rows of a query tile and keys of a key tile
-constexpr int kBwdThreads = 192;
-constexpr int kEwThreads = 128;     // elementwise warpgroup
-constexpr int kBwdProducerWarp = 4, kBwdIssuerWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kEwThreads = 128;     // one elementwise warpgroup (two of them: warps 0-3, 4-7)
+constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzled sub-tile
 constexpr uint64_t kBwdDrainNs = 100000000ull;
@@ -40,6 +47,10 @@ constexpr uint64_t kBwdDrainNs = 100000000ull;
 struct BwdParams {
   const float* lse2;  // [B*Hq, nqp]  L * log2(e); +inf on padding rows
   const float* dvec;  // [B*Hq, nqp]  D; 0 on padding rows
+  const uint16_t* q;     // [B, Hq, N_q, d]
+  const uint16_t* k;     // [B, Hkv, N_kv, d]
+  const uint16_t* v;
+  const uint16_t* dout;  // [B, Hq, N_q, d]
   uint16_t* dq;       // [B, Hq, N_q, d]
   uint16_t* dk;       // [B, Hkv, N_kv, d]
   uint16_t* dv;
@@ -93,29 +104,6 @@ __device__ __forceinline__ void store_zero_row(uint16_t* dst) {
   for (int c = 0; c < D / 8; ++c) out[c] = make_uint4(0, 0, 0, 0);
 }
 
-// K-major A x K-major B^T, both 128 rows x D (the two 64-column halves of d are separate swizzled
-// sub-tiles): D[128 x 128] (+)= A B^T.
-template <int D>
-__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                              uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-    mma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
-           idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
-// A [128 x 128] in tensor memory (16-bit pairs, 64 columns) times B [128 rows x D] in shared
-// memory read MN-major: D[128 x D] (+)= A B.
-__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                              uint32_t idesc, bool accumulate) {
-#pragma unroll
-  for (int kk = 0; kk < kBT / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 16 * 128, kSub, 1024), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-}
-
 }  // namespace
 
 // ------------------------------------------------------------------------------------------
@@ -152,6 +140,11 @@ __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, con
 // ------------------------------------------------------------------------------------------
 // kernel 1: dK, dV of one 128-key tile
 // ------------------------------------------------------------------------------------------
+// Tensor memory: S^T 0-127, dP^T 128-255, dV 256-(256+d), dK after it.  The two elementwise
+// warpgroups split the 128 queries of a tile (warpgroup w: queries 64w .. 64w+63); each writes
+// P^T and then dS^T as 16-bit pairs into the S^T columns it has already read (P^T of warpgroup
+// w at columns 64w .. 64w+31, dS^T at 64w+32 .. 64w+63), so that dP^T is free as soon as it has
+// been read and the next tile's dP^T runs during this tile's dS^T step.
 template <int D, int QS>
 struct KvLayout {
   static constexpr uint32_t kTile = kBT * D * 2;
@@ -160,14 +153,39 @@ struct KvLayout {
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
-  // kv_full, st_full[QS], st_empty[QS], s_full, dp_full, p_ready, ds_ready, p_done, ds_done,
-  // drain
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 7;
+  // kv_full, st_full[QS], st_empty[QS], s_full, dp_full, p_ready, dp_free, ds_ready, drain
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 6;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tile alignment");
   static_assert(kBytes <= 232448, "shared memory per block");
 };
+
+// K-major A x K-major B^T, both 128 rows x D (the two 64-column halves of d are separate swizzled
+// sub-tiles): D[128 x 128] (+)= A B^T.
+template <int D>
+__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                              uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+    mma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// A [128 x 128] in tensor memory as 16-bit pairs, the first 64 of its K elements at columns
+// a_tmem .. +31 and the second 64 at a_tmem + 64 .. +95 (one half per elementwise warpgroup),
+// times B [128 rows x D] in shared memory read MN-major: D[128 x D] (+)= A B.
+__device__ __forceinline__ void mma_split_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                               uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBT / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+           make_sdesc_sw128(b_smem + kk * 16 * 128, kSub, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
 
 template <int D, bool BF16, int QS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -186,11 +204,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #define ST_EMPTY(s) (bars + 8u * (1 + QS + (s)))
   const uint32_t bar_s = bars + 8u * (1 + 2 * QS);  // S^T_i written (MMA commit)
   const uint32_t bar_dp = bar_s + 8;                 // dP^T_i written (MMA commit)
-  const uint32_t bar_p = bar_s + 16;                 // P^T_i stored over S^T (128 arrivals)
-  const uint32_t bar_ds = bar_s + 24;                // dS^T_i stored over dP^T (128 arrivals)
-  const uint32_t bar_pdone = bar_s + 32;             // dV += P^T_i dO_i finished: S^T free
-  const uint32_t bar_dsdone = bar_s + 40;            // dK += dS^T_i Q_i finished: dP^T free
-  const uint32_t bar_drain = bar_s + 48;
+  const uint32_t bar_p = bar_s + 16;                 // P^T_i stored (256 arrivals)
+  const uint32_t bar_dpfree = bar_s + 24;            // dP^T_i read (256 arrivals)
+  const uint32_t bar_ds = bar_s + 32;                // dS^T_i stored (256 arrivals)
+  const uint32_t bar_drain = bar_s + 40;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -221,10 +238,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_p, kEwThreads);
-    mbar_init(bar_ds, kEwThreads);
-    mbar_init(bar_pdone, 1);
-    mbar_init(bar_dsdone, 1);
+    mbar_init(bar_p, 2 * kEwThreads);
+    mbar_init(bar_dpfree, 2 * kEwThreads);
+    mbar_init(bar_ds, 2 * kEwThreads);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -237,7 +253,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 
   if (warp == kBwdProducerWarp) {
     if (lane == 0 && n > 0) {
@@ -278,40 +293,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
-      constexpr uint32_t idesc_tr = make_idesc_f16(BF16, kBT, D, true);
-      // Per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; once P^T_i is stored,
-      // dV += P^T_i dO_i; once dS^T_i is stored, dK += dS^T_i Q_i.  The next tile's S^T waits
-      // only for the dV MMA (which read P^T over S^T) and its dP^T for the dK MMA, so the tensor
-      // pipe runs dV_i, dK_i, S^T_{i+1}, dP^T_{i+1} back to back while the elementwise warps
-      // work on the other half of the tile pair.
-      auto issue_sdp = [&](int i) -> bool {
+      constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
+      // Per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; dV += P^T_i dO_i once P^T_i is
+      // stored; dK += dS^T_i Q_i once dS^T_i is stored; then dP^T_{i+1} (dP^T_i has been read)
+      // and S^T_{i+1}, which overwrites the columns dV_i and dK_i read (the MMAs of one thread
+      // run in issue order).
+      auto issue_s = [&](int i) -> bool {
         const int s = i % QS;
-        const uint32_t st = base + L::kStages + s * L::kStage;
         if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
-        if (i > 0 && !wait_bounded(bar_pdone, (i - 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + kColS, base + L::kK, st, idesc_rr);  // S^T = K Q^T
+        mma_rows_rows<D>(tmem + L::kColS, base + L::kK, base + L::kStages + s * L::kStage, idesc_rr);
         mma_commit(bar_s);
-        if (i > 0 && !wait_bounded(bar_dsdone, (i - 1) & 1, abort_flag, p.status)) return false;
+        return true;
+      };
+      auto issue_dp = [&](int i) -> bool {
+        const int s = i % QS;
+        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + kColDP, base + L::kV, st + L::kTile, idesc_rr);  // dP^T = V dO^T
+        mma_rows_rows<D>(tmem + L::kColDP, base + L::kV,
+                         base + L::kStages + s * L::kStage + L::kTile, idesc_rr);
         mma_commit(bar_dp);
         return true;
       };
-      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_sdp(0);
+      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_s(0) && issue_dp(0);
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % QS;
         const uint32_t st = base + L::kStages + s * L::kStage;
         if (!wait_bounded(bar_p, i & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_tmem_rows(tmem + kColDV, tmem + kColS, st + L::kTile, idesc_tr, i > 0);  // dV += P^T dO
-        mma_commit(bar_pdone);
+        mma_split_rows(tmem + L::kColDV, tmem + L::kColS, st + L::kTile, idesc_acc, i > 0);  // dV
         if (!wait_bounded(bar_ds, i & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_tmem_rows(tmem + kColDK, tmem + kColDP, st, idesc_tr, i > 0);  // dK += dS^T Q
-        mma_commit(bar_dsdone);
+        mma_split_rows(tmem + L::kColDK, tmem + L::kColS + 32, st, idesc_acc, i > 0);  // dK
         mma_commit(ST_EMPTY(s));
-        if (i + 1 < n) ok = issue_sdp(i + 1);
+        // dP^T_{i+1} then S^T_{i+1}: as late as the elementwise step allows (it needs both
+        // only after dS^T_i), which gives the load of stage i + 1 (freed by dK_{i-1}) time
+        if (!wait_bounded(bar_dpfree, i & 1, abort_flag, p.status)) break;
+        if (i + 1 < n && !issue_dp(i + 1)) break;
+        if (i + 1 < n) ok = issue_s(i + 1);
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -319,48 +338,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = key)
+    // Warpgroup w takes queries c0 = 64w .. c0+63 of every query tile; thread r owns key row r
+    // (warp % 4 is its tensor-memory lane quarter).
+    const int wg = warp >> 2;
+    const int c0 = wg * 64;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int kr = kt * kBT + r;  // this thread's key
     const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.sl2, scale = p.scale;
+    const int q_first_visible = kr - off;  // the smallest query row that sees this key
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int s = i % QS;
       const int qt = qt_lo + i % nq_per;
-      const float* lv = reinterpret_cast<const float*>(gbase + L::kStages + s * L::kStage + 2 * L::kTile);
+      const float* lv = reinterpret_cast<const float*>(gbase + L::kStages + s * L::kStage +
+                                                       2 * L::kTile) + c0;
       const float* dvv = lv + kBT;
-      const int q_first_visible = kr - off;  // the smallest query row that sees this key
-      // P^T row of this key over the tile's 128 queries, kept in registers for dS^T
-      float pv[kBT];
+      const int q0 = qt * kBT + c0;
       if (!ew_wait(bar_s, i & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // P^T row of this key over the warpgroup's 64 queries, kept in registers for dS^T
+      float pv[64];
+      uint32_t pp[32];
 #pragma unroll
-      for (int c4 = 0; c4 < kBT / 32; ++c4) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t sv[32];
-        tmem_ld32(row_tmem + kColS + c4 * 32, sv);
+        tmem_ld32(row_tmem + L::kColS + c0 + h * 32, sv);
         tmem_wait_ld();
-        uint32_t pp[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const int col = c4 * 32 + e;
+          const int col = h * 32 + e;
           const float4 l4 = *reinterpret_cast<const float4*>(lv + col);
-          const int qrow = qt * kBT + col;
-          const bool causal = p.causal;
           const float la[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const bool vis = !causal || qrow + u >= q_first_visible;
+            const bool vis = !p.causal || q0 + col + u >= q_first_visible;
             pv[col + u] = vis ? ex2(fmaf(__uint_as_float(sv[e + u]), sl2, -la[u])) : 0.0f;
           }
-          pp[(e >> 1)] = pack2<BF16>(pv[col], pv[col + 1]);
-          pp[(e >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
+          pp[col >> 1] = pack2<BF16>(pv[col], pv[col + 1]);
+          pp[(col >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
         }
-        tmem_st16(row_tmem + kColS + c4 * 16, pp);  // in place: chunks already read
       }
+      tmem_st32(row_tmem + L::kColS + c0, pp);  // P^T over the S^T columns already read
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_p);
@@ -369,41 +392,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
+      uint32_t dpv[2][32];
+      tmem_ld32(row_tmem + L::kColDP + c0, dpv[0]);
+      tmem_ld32(row_tmem + L::kColDP + c0 + 32, dpv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_dpfree);  // dP^T_{i+1} may overwrite
+      uint32_t dd[32];
 #pragma unroll
-      for (int c4 = 0; c4 < kBT / 32; ++c4) {
-        uint32_t dpv[32];
-        tmem_ld32(row_tmem + kColDP + c4 * 32, dpv);
-        tmem_wait_ld();
-        uint32_t dd[16];
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const int col = c4 * 32 + e;
+          const int col = h * 32 + e;
           const float4 d4 = *reinterpret_cast<const float4*>(dvv + col);
-          dd[e >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[e]) - d4.x) * scale,
-                                   pv[col + 1] * (__uint_as_float(dpv[e + 1]) - d4.y) * scale);
-          dd[(e >> 1) + 1] = pack2<BF16>(pv[col + 2] * (__uint_as_float(dpv[e + 2]) - d4.z) * scale,
-                                         pv[col + 3] * (__uint_as_float(dpv[e + 3]) - d4.w) * scale);
+          dd[col >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[h][e]) - d4.x) * scale,
+                                     pv[col + 1] * (__uint_as_float(dpv[h][e + 1]) - d4.y) * scale);
+          dd[(col >> 1) + 1] =
+              pack2<BF16>(pv[col + 2] * (__uint_as_float(dpv[h][e + 2]) - d4.z) * scale,
+                          pv[col + 3] * (__uint_as_float(dpv[h][e + 3]) - d4.w) * scale);
         }
-        tmem_st16(row_tmem + kColDP + c4 * 16, dd);
-      }
+      tmem_st32(row_tmem + L::kColS + c0 + 32, dd);  // dS^T beside this warpgroup's P^T
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ds);
     }
-    // epilogue: dV and dK rows of this key tile
-    // the last dK MMA finished means every MMA of the block has (they complete in issue order)
-    if (ok && n > 0) ok = ew_wait(bar_dsdone, (n - 1) & 1, abort_flag, p.status);
+    // epilogue: warpgroup 0 stores dV, warpgroup 1 dK, once the last MMA has finished
+    if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const bool store = kr < p.N_kv;
       const size_t grow = (static_cast<size_t>(bkv) * p.N_kv + (store ? kr : 0)) * D;
-      if (n > 0) {
-        store_acc_row<D, BF16>(row_tmem + kColDV, p.dv + grow, store);
-        store_acc_row<D, BF16>(row_tmem + kColDK, p.dk + grow, store);
-      } else if (store) {
-        store_zero_row<D>(p.dv + grow);
-        store_zero_row<D>(p.dk + grow);
-      }
+      uint16_t* dst = (wg ? p.dk : p.dv) + grow;
+      if (n > 0)
+        store_acc_row<D, BF16>(row_tmem + (wg ? L::kColDK : L::kColDV), dst, store);
+      else if (store)
+        store_zero_row<D>(dst);
     }
   }
 #undef ST_FULL
@@ -419,29 +442,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ------------------------------------------------------------------------------------------
 // kernel 2: dQ of one 128-row query tile
 // ------------------------------------------------------------------------------------------
-template <int D, int KS>
+// Tensor memory: S[2] 0-255 (double-buffered), dP 256-383, dQ 384-.  The two elementwise
+// warpgroups split the 128 keys of a tile (warpgroup w: keys 64w .. 64w+63); each keeps its P
+// in registers and writes dS as 16-bit pairs over the S columns it has read (64w .. 64w+31 of
+// the tile's S buffer), so that dP is free as soon as it has been read.
+template <int D, int KR, int VR>
 struct QLayout {
   static constexpr uint32_t kTile = kBT * D * 2;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kDO = kTile;
-  static constexpr uint32_t kK = 2 * kTile;            // K ring, KS slots
-  static constexpr uint32_t kV = kK + KS * kTile;      // V ring, KS slots
-  static constexpr uint32_t kBar = kV + KS * kTile;
-  // q_full, k_full[KS], k_empty[KS], v_full[KS], v_empty[KS], sdp_full, s_free[2], ds_ready,
-  // dq_done, drain
-  static constexpr uint32_t kNumBars = 1 + 4 * KS + 6;
+  static constexpr uint32_t kK = 2 * kTile;          // K ring, KR slots
+  static constexpr uint32_t kV = kK + KR * kTile;    // V ring, VR slots
+  static constexpr uint32_t kBar = kV + VR * kTile;
+  // q_full, k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], s_full[2], dp_full, dp_free,
+  // ds_ready[2], drain
+  static constexpr uint32_t kNumBars = 1 + 2 * KR + 2 * VR + 7;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
   static_assert(kBytes <= 232448, "shared memory per block");
 };
 
-template <int D, bool BF16, int KS>
+template <int D, bool BF16, int KR, int VR>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-  using L = QLayout<D, KS>;
+  using L = QLayout<D, KR, VR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -449,14 +477,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bars = base + L::kBar;
   const uint32_t bar_q = bars;
 #define K_FULL(s) (bars + 8u * (1 + (s)))
-#define K_EMPTY(s) (bars + 8u * (1 + KS + (s)))
-#define V_FULL(s) (bars + 8u * (1 + 2 * KS + (s)))
-#define V_EMPTY(s) (bars + 8u * (1 + 3 * KS + (s)))
-  const uint32_t bar_sdp = bars + 8u * (1 + 4 * KS);
-#define S_FREE(b) (bar_sdp + 8u * (1 + (b)))
-  const uint32_t bar_ds = bar_sdp + 24;
-  const uint32_t bar_dq = bar_sdp + 32;
-  const uint32_t bar_drain = bar_sdp + 40;
+#define K_EMPTY(s) (bars + 8u * (1 + KR + (s)))
+#define V_FULL(s) (bars + 8u * (1 + 2 * KR + (s)))
+#define V_EMPTY(s) (bars + 8u * (1 + 2 * KR + VR + (s)))
+  const uint32_t bar_sfull = bars + 8u * (1 + 2 * KR + 2 * VR);  // [2] S_t in buffer t % 2
+  const uint32_t bar_dp = bar_sfull + 16;               // dP_t written (commit)
+  const uint32_t bar_dpfree = bar_sfull + 24;           // dP_t read (256 arrivals)
+  const uint32_t bar_ds = bar_sfull + 32;               // [2] dS_t stored in buffer t % 2
+  const uint32_t bar_drain = bar_sfull + 48;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -471,17 +499,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < KR; ++s) {
       mbar_init(K_FULL(s), 1);
       mbar_init(K_EMPTY(s), 1);
+    }
+    for (int s = 0; s < VR; ++s) {
       mbar_init(V_FULL(s), 1);
       mbar_init(V_EMPTY(s), 1);
     }
-    mbar_init(bar_sdp, 1);
-    mbar_init(S_FREE(0), kEwThreads);
-    mbar_init(S_FREE(1), kEwThreads);
-    mbar_init(bar_ds, kEwThreads);
-    mbar_init(bar_dq, 1);
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(bar_sfull + 8u * bb, 1);
+      mbar_init(bar_ds + 8u * bb, 2 * kEwThreads);
+    }
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_dpfree, 2 * kEwThreads);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -494,8 +525,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S double-buffered, one dP buffer (dS written over it), the dQ accumulator
-  constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
 
   if (warp == kBwdProducerWarp) {
     if (lane == 0 && n > 0) {
@@ -509,63 +538,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(base + L::kQ + sub * kSub, &tm_q, bar_q, sub * 64, qt * kBT, bh);
         tma_load_3d(base + L::kDO + sub * kSub, &tm_do, bar_q, sub * 64, qt * kBT, bh);
       }
-      int issued = 0;
+      // K_t goes to K slot t % KR (freed by dQ_{t-KR}), V_t to V slot t % VR (freed by
+      // dP_{t-VR}, which comes much earlier): the K ring is the deeper one, so that S_{t+2},
+      // issued right after dQ_t, finds K_{t+2} loaded.
+      int issued_k = 0, issued_v = 0;
       for (int t = 0; t < n; ++t) {
-        const int s = t % KS;
-        if (t >= KS && !wait_bounded(K_EMPTY(s), ((t / KS) - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(K_FULL(s), L::kTile);
+        const int sk = t % KR, sv = t % VR;
+        if (t >= KR && !wait_bounded(K_EMPTY(sk), ((t / KR) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(K_FULL(sk), L::kTile);
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_3d(base + L::kK + s * L::kTile + sub * kSub, &tm_k, K_FULL(s), sub * 64, t * kBT,
-                      kv_plane);
-        if (t >= KS && !wait_bounded(V_EMPTY(s), ((t / KS) - 1) & 1, abort_flag, p.status)) {
-          issued = t + 1;  // K_t is in flight
-          break;
-        }
-        mbar_arrive_expect_tx(V_FULL(s), L::kTile);
+          tma_load_3d(base + L::kK + sk * L::kTile + sub * kSub, &tm_k, K_FULL(sk), sub * 64,
+                      t * kBT, kv_plane);
+        issued_k = t + 1;
+        if (t >= VR && !wait_bounded(V_EMPTY(sv), ((t / VR) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(V_FULL(sv), L::kTile);
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_3d(base + L::kV + s * L::kTile + sub * kSub, &tm_v, V_FULL(s), sub * 64, t * kBT,
-                      kv_plane);
-        issued = t + 1;
+          tma_load_3d(base + L::kV + sv * L::kTile + sub * kSub, &tm_v, V_FULL(sv), sub * 64,
+                      t * kBT, kv_plane);
+        issued_v = t + 1;
       }
       wait_bounded(bar_q, 0, nullptr, p.status, kBwdDrainNs);
-      for (int t = (issued > KS ? issued - KS : 0); t < issued; ++t) {
-        wait_bounded(K_FULL(t % KS), (t / KS) & 1, nullptr, p.status, kBwdDrainNs);
-        wait_bounded(V_FULL(t % KS), (t / KS) & 1, nullptr, p.status, kBwdDrainNs);
-      }
+      for (int t = (issued_k > KR ? issued_k - KR : 0); t < issued_k; ++t)
+        wait_bounded(K_FULL(t % KR), (t / KR) & 1, nullptr, p.status, kBwdDrainNs);
+      for (int t = (issued_v > VR ? issued_v - VR : 0); t < issued_v; ++t)
+        wait_bounded(V_FULL(t % VR), (t / VR) & 1, nullptr, p.status, kBwdDrainNs);
     }
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
-      constexpr uint32_t idesc_tr = make_idesc_f16(BF16, kBT, D, true);
-      // S_t = Q K_t^T into S buffer t % 2 once the elementwise step of tile t - 2 has read it
+      constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
+      // S_t = Q K_t^T into buffer t % 2 (next written by S_{t+2}, issued after dQ_t, which
+      // reads dS_t there); dP_t = dO V_t^T once dP_{t-1} has been read; dQ += dS_t K_t.
       auto issue_s = [&](int t) -> bool {
-        if (t >= 2 && !wait_bounded(S_FREE(t & 1), ((t >> 1) - 1) & 1, abort_flag, p.status))
-          return false;
-        if (!wait_bounded(K_FULL(t % KS), (t / KS) & 1, abort_flag, p.status)) return false;
+        const int s = t % KR;
+        if (!wait_bounded(K_FULL(s), (t / KR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + ((t & 1) ? kColS1 : kColS0), base + L::kQ,
-                         base + L::kK + (t % KS) * L::kTile, idesc_rr);
+        mma_rows_rows<D>(tmem + L::kColS + (t & 1) * 128, base + L::kQ, base + L::kK + s * L::kTile,
+                         idesc_rr);
+        mma_commit(bar_sfull + 8u * (t & 1));
         return true;
       };
-      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) && issue_s(0);
-      for (int t = 0; ok && t < n; ++t) {
-        const int s = t % KS;
-        // dP_t = dO V_t^T, once dQ += dS_{t-1} K_{t-1} has read the dP buffer
-        if (t > 0 && !wait_bounded(bar_dq, (t - 1) & 1, abort_flag, p.status)) break;
-        if (!wait_bounded(V_FULL(s), (t / KS) & 1, abort_flag, p.status)) break;
+      auto issue_dp = [&](int t) -> bool {
+        const int s = t % VR;
+        if (!wait_bounded(V_FULL(s), (t / VR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + kColDP, base + L::kDO, base + L::kV + s * L::kTile, idesc_rr);
-        mma_commit(bar_sdp);     // S_t and dP_t ready
+        mma_rows_rows<D>(tmem + L::kColDP, base + L::kDO, base + L::kV + s * L::kTile, idesc_rr);
+        mma_commit(bar_dp);
         mma_commit(V_EMPTY(s));
-        if (t + 1 < n && !issue_s(t + 1)) break;  // overlaps the elementwise step of tile t
-        if (!wait_bounded(bar_ds, t & 1, abort_flag, p.status)) break;
+        return true;
+      };
+      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) && issue_s(0) && issue_dp(0) &&
+                (n < 2 || issue_s(1));
+      for (int t = 0; ok && t < n; ++t) {
+        const int s = t % KR;
+        if (!wait_bounded(bar_dpfree, t & 1, abort_flag, p.status)) break;
+        if (t + 1 < n && !issue_dp(t + 1)) break;
+        if (!wait_bounded(bar_ds + 8u * (t & 1), (t >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_tmem_rows(tmem + kColDQ, tmem + kColDP, base + L::kK + s * L::kTile, idesc_tr, t > 0);
-        mma_commit(bar_dq);
+        mma_split_rows(tmem + L::kColDQ, tmem + L::kColS + (t & 1) * 128,
+                       base + L::kK + s * L::kTile, idesc_q, t > 0);  // dQ += dS K
         mma_commit(K_EMPTY(s));
+        if (t + 2 < n) ok = issue_s(t + 2);
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -573,6 +609,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = query)
+    // Warpgroup w takes keys c0 = 64w .. c0+63 of every key tile; thread r owns query row r.
+    const int wg = warp >> 2;
+    const int c0 = wg * 64;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int row = qt * kBT + r;
@@ -585,43 +624,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lim > p.N_kv - 1) lim = p.N_kv - 1;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
-      if (!ew_wait(bar_sdp, t & 1, abort_flag, p.status)) {
+      const uint32_t s_col = L::kColS + (t & 1) * 128 + c0;
+      const bool masked = t >= first_masked;
+      const int rel = lim - (t * kBT + c0);  // last visible key, relative to this half tile
+      if (!ew_wait(bar_sfull + 8u * (t & 1), (t >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_col = (t & 1) ? kColS1 : kColS0;
-      const bool masked = t >= first_masked;
-      const int rel = lim - t * kBT;
-#pragma unroll 1
-      for (int c4 = 0; c4 < kBT / 32; ++c4) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(row_tmem + s_col + c4 * 32, sv);
-        tmem_ld32(row_tmem + kColDP + c4 * 32, dpv);
+      float pv[64];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sv[32];
+        tmem_ld32(row_tmem + s_col + h * 32, sv);
         tmem_wait_ld();
-        uint32_t dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = h * 32 + e;
+          pv[col] = (!masked || col <= rel) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.0f;
+        }
+      }
+      if (!ew_wait(bar_dp, t & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t dpv[2][32];
+      tmem_ld32(row_tmem + L::kColDP + c0, dpv[0]);
+      tmem_ld32(row_tmem + L::kColDP + c0 + 32, dpv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_dpfree);  // dP_{t+1} may overwrite
+      uint32_t dd[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c = c4 * 32 + e;
-          const float pa = (!masked || c <= rel) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.0f;
-          const float pb = (!masked || c + 1 <= rel) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.0f;
-          dd[e >> 1] = pack2<BF16>(pa * (__uint_as_float(dpv[e]) - dr) * scale,
-                                   pb * (__uint_as_float(dpv[e + 1]) - dr) * scale);
+          const int col = h * 32 + e;
+          dd[col >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[h][e]) - dr) * scale,
+                                     pv[col + 1] * (__uint_as_float(dpv[h][e + 1]) - dr) * scale);
         }
-        tmem_st16(row_tmem + kColDP + c4 * 16, dd);  // in place over dP chunks already read
-      }
+      tmem_st32(row_tmem + s_col, dd);  // dS over the S columns already read
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(S_FREE(t & 1));
-      mbar_arrive(bar_ds);
+      mbar_arrive(bar_ds + 8u * (t & 1));
     }
-    if (ok && n > 0) ok = ew_wait(bar_dq, (n - 1) & 1, abort_flag, p.status);
-    if (ok) {
+    if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
+    if (ok && wg == 0) {
       tc_fence_after();
       const bool store = row < p.N_q;
       const size_t grow = (static_cast<size_t>(bh) * p.N_q + (store ? row : 0)) * D;
       if (n > 0)
-        store_acc_row<D, BF16>(row_tmem + kColDQ, p.dq + grow, store);
+        store_acc_row<D, BF16>(row_tmem + L::kColDQ, p.dq + grow, store);
       else if (store)
         store_zero_row<D>(p.dq + grow);
     }
@@ -630,7 +684,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #undef K_EMPTY
 #undef V_FULL
 #undef V_EMPTY
-#undef S_FREE
   tc_fence_before();
   __syncthreads();
   if (warp == kBwdIssuerWarp) {
@@ -650,10 +703,11 @@ size_t bwd_workspace_bytes(int B, int Hq, int N_q) {
 
 template <int D, bool BF16>
 static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
-  constexpr int QS = (D == 128) ? 2 : 3;
-  constexpr int KS = (D == 128) ? 2 : 3;
+  constexpr int QS = (D == 128) ? 2 : 4;  // query-tile stages of the dK/dV kernel
+  constexpr int KR = (D == 128) ? 3 : 4;  // K slots of the dQ kernel
+  constexpr int VR = (D == 128) ? 2 : 4;  // V slots of the dQ kernel
   using LK = KvLayout<D, QS>;
-  using LQ = QLayout<D, KS>;
+  using LQ = QLayout<D, KR, VR>;
   const uint64_t bhq = static_cast<uint64_t>(a.B) * a.Hq;
   const uint64_t bhk = static_cast<uint64_t>(a.B) * a.Hkv;
   const uint64_t rb = static_cast<uint64_t>(D) * 2;
@@ -668,6 +722,10 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const int nqp = n_qtiles * kBT;
   p.lse2 = static_cast<const float*>(a.workspace);
   p.dvec = p.lse2 + bhq * nqp;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k = static_cast<const uint16_t*>(a.k);
+  p.v = static_cast<const uint16_t*>(a.v);
+  p.dout = static_cast<const uint16_t*>(a.dout);
   p.dq = static_cast<uint16_t*>(a.dq);
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
@@ -690,7 +748,7 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
       const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), a.N_q, nqp, rows);
   if (cudaGetLastError() != cudaSuccess) return -5;
   auto kkv = attn_bwd_dkdv_kernel<D, BF16, QS>;
-  auto kq = attn_bwd_dq_kernel<D, BF16, KS>;
+  auto kq = attn_bwd_dq_kernel<D, BF16, KR, VR>;
   if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, LK::kBytes) != cudaSuccess ||
       cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kBytes) != cudaSuccess)
     return -5;
