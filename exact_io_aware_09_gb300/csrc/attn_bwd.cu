@@ -45,8 +45,8 @@ constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzle
 constexpr uint64_t kBwdDrainNs = 100000000ull;
 
 struct BwdParams {
-  const float* lse2;  // [B*Hq, nqp]  L * log2(e); +inf on padding rows
-  const float* dvec;  // [B*Hq, nqp]  D; 0 on padding rows
+  const float* lse2;  // [B*Hq, nqp]  -L * log2(e); -inf on padding rows
+  const float* dvec;  // [B*Hq, nqp]  -scale * D; 0 on padding rows
   const uint16_t* q;     // [B, Hq, N_q, d]
   const uint16_t* k;     // [B, Hkv, N_kv, d]
   const uint16_t* v;
@@ -107,11 +107,12 @@ __device__ __forceinline__ void store_zero_row(uint16_t* dst) {
 }  // namespace
 
 // ------------------------------------------------------------------------------------------
-// kernel 0: D = rowsum(dO o O) and L log2(e), one warp per (padded) query row
+// kernel 0: -scale D = -scale rowsum(dO o O) and -L log2(e), one warp per (padded) query row
 // ------------------------------------------------------------------------------------------
 template <int D, bool BF16>
 __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
-                                    float* lse2, float* dvec, int N_q, int nqp, long long rows) {
+                                    float* lse2, float* dvec, int N_q, int nqp, long long rows,
+                                    float scale) {
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
@@ -132,8 +133,10 @@ __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, con
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
   if (lane == 0) {
-    dvec[w] = (i < N_q) ? acc : 0.0f;
-    lse2[w] = (i < N_q) ? lse[bh * N_q + i] * 1.4426950408889634f : INFINITY;
+    // stored negated (and D times the scale), so that the elementwise steps are single FMAs:
+    // s * scale log2(e) + (-L log2(e)) and dP * scale + (-scale D)
+    dvec[w] = (i < N_q) ? -scale * acc : 0.0f;
+    lse2[w] = (i < N_q) ? -lse[bh * N_q + i] * 1.4426950408889634f : -INFINITY;
   }
 }
 
@@ -361,27 +364,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      // P^T row of this key over the warpgroup's 64 queries, kept in registers for dS^T
+      // P^T row of this key over the warpgroup's 64 queries, kept in registers for dS^T:
+      // p = 2^(s scale log2(e) - L log2(e)), one packed FMA per pair; the causal test only
+      // where some query of the 64 precedes this key
       float pv[64];
       uint32_t pp[32];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32];
-        tmem_ld32(row_tmem + L::kColS + c0 + h * 32, sv);
+      {
+        uint32_t sv[2][32];
+        tmem_ld32(row_tmem + L::kColS + c0, sv[0]);
+        tmem_ld32(row_tmem + L::kColS + c0 + 32, sv[1]);
         tmem_wait_ld();
+        const bool full = !p.causal || q0 >= q_first_visible;
+        const bool all_full = __all_sync(0xffffffffu, full);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int col = h * 32 + e;
-          const float4 l4 = *reinterpret_cast<const float4*>(lv + col);
-          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const bool vis = !p.causal || q0 + col + u >= q_first_visible;
-            pv[col + u] = vis ? ex2(fmaf(__uint_as_float(sv[e + u]), sl2, -la[u])) : 0.0f;
+          for (int e = 0; e < 32; e += 4) {
+            const int col = h * 32 + e;
+            const float4 l4 = *reinterpret_cast<const float4*>(lv + col);
+            float a0, a1, a2, a3;
+            fma2(a0, a1, __uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1]), sl2, sl2, l4.x, l4.y);
+            fma2(a2, a3, __uint_as_float(sv[h][e + 2]), __uint_as_float(sv[h][e + 3]), sl2, sl2, l4.z,
+                 l4.w);
+            if (!all_full) {
+              const int rel = q_first_visible - (q0 + col);  // columns below rel precede the key
+              a0 = (0 >= rel) ? a0 : -INFINITY;
+              a1 = (1 >= rel) ? a1 : -INFINITY;
+              a2 = (2 >= rel) ? a2 : -INFINITY;
+              a3 = (3 >= rel) ? a3 : -INFINITY;
+            }
+            pv[col] = ex2(a0);
+            pv[col + 1] = ex2(a1);
+            pv[col + 2] = ex2(a2);
+            pv[col + 3] = ex2(a3);
+            pp[col >> 1] = pack2<BF16>(pv[col], pv[col + 1]);
+            pp[(col >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
           }
-          pp[col >> 1] = pack2<BF16>(pv[col], pv[col + 1]);
-          pp[(col >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
-        }
       }
       tmem_st32(row_tmem + L::kColS + c0, pp);  // P^T over the S^T columns already read
       tmem_wait_st();
@@ -398,6 +416,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar_dpfree);  // dP^T_{i+1} may overwrite
+      // dS^T = P^T o (dP^T - D) scale = P^T o (dP^T scale + (-scale D)): two packed FMAs a pair
       uint32_t dd[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -405,11 +424,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 32; e += 4) {
           const int col = h * 32 + e;
           const float4 d4 = *reinterpret_cast<const float4*>(dvv + col);
-          dd[col >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[h][e]) - d4.x) * scale,
-                                     pv[col + 1] * (__uint_as_float(dpv[h][e + 1]) - d4.y) * scale);
-          dd[(col >> 1) + 1] =
-              pack2<BF16>(pv[col + 2] * (__uint_as_float(dpv[h][e + 2]) - d4.z) * scale,
-                          pv[col + 3] * (__uint_as_float(dpv[h][e + 3]) - d4.w) * scale);
+          float u0, u1, u2, u3, g0, g1, g2, g3;
+          fma2(u0, u1, __uint_as_float(dpv[h][e]), __uint_as_float(dpv[h][e + 1]), scale, scale, d4.x, d4.y);
+          fma2(u2, u3, __uint_as_float(dpv[h][e + 2]), __uint_as_float(dpv[h][e + 3]), scale, scale, d4.z,
+               d4.w);
+          fma2(g0, g1, pv[col], pv[col + 1], u0, u1, 0.0f, 0.0f);
+          fma2(g2, g3, pv[col + 2], pv[col + 3], u2, u3, 0.0f, 0.0f);
+          dd[col >> 1] = pack2<BF16>(g0, g1);
+          dd[(col >> 1) + 1] = pack2<BF16>(g2, g3);
         }
       tmem_st32(row_tmem + L::kColS + c0 + 32, dd);  // dS^T beside this warpgroup's P^T
       tmem_wait_st();
@@ -617,8 +639,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = qt * kBT + r;
     const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const size_t vec = static_cast<size_t>(bh) * p.nqp + row;
-    const float lse2 = p.lse2[vec];
-    const float dr = p.dvec[vec];
+    const float nl2 = p.lse2[vec];  // -L log2(e)
+    const float nsd = p.dvec[vec];  // -scale D
     const float sl2 = p.sl2, scale = p.scale;
     int lim = p.causal ? row + (p.N_kv - p.N_q) : p.N_kv - 1;  // last visible key of this row
     if (lim > p.N_kv - 1) lim = p.N_kv - 1;
@@ -632,17 +654,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
+      // p = 2^(s scale log2(e) - L log2(e)), one packed FMA a pair; the mask only on the tiles
+      // that need it (the same for every row of the tile)
       float pv[64];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32];
-        tmem_ld32(row_tmem + s_col + h * 32, sv);
+      {
+        uint32_t sv[2][32];
+        tmem_ld32(row_tmem + s_col, sv[0]);
+        tmem_ld32(row_tmem + s_col + 32, sv[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = h * 32 + e;
-          pv[col] = (!masked || col <= rel) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.0f;
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = h * 32 + e;
+            float a0, a1;
+            fma2(a0, a1, __uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1]), sl2, sl2, nl2, nl2);
+            if (masked) {
+              a0 = (col <= rel) ? a0 : -INFINITY;
+              a1 = (col + 1 <= rel) ? a1 : -INFINITY;
+            }
+            pv[col] = ex2(a0);
+            pv[col + 1] = ex2(a1);
+          }
       }
       if (!ew_wait(bar_dp, t & 1, abort_flag, p.status)) {
         ok = false;
@@ -655,14 +688,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar_dpfree);  // dP_{t+1} may overwrite
+      // dS = P o (dP scale + (-scale D)): two packed FMAs a pair
       uint32_t dd[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = h * 32 + e;
-          dd[col >> 1] = pack2<BF16>(pv[col] * (__uint_as_float(dpv[h][e]) - dr) * scale,
-                                     pv[col + 1] * (__uint_as_float(dpv[h][e + 1]) - dr) * scale);
+          float u0, u1, g0, g1;
+          fma2(u0, u1, __uint_as_float(dpv[h][e]), __uint_as_float(dpv[h][e + 1]), scale, scale, nsd, nsd);
+          fma2(g0, g1, pv[col], pv[col + 1], u0, u1, 0.0f, 0.0f);
+          dd[col >> 1] = pack2<BF16>(g0, g1);
         }
       tmem_st32(row_tmem + s_col, dd);  // dS over the S columns already read
       tmem_wait_st();
@@ -745,7 +781,7 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(bhq) * nqp;
   attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse,
-      const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), a.N_q, nqp, rows);
+      const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), a.N_q, nqp, rows, a.scale);
   if (cudaGetLastError() != cudaSuccess) return -5;
   auto kkv = attn_bwd_dkdv_kernel<D, BF16, QS>;
   auto kq = attn_bwd_dq_kernel<D, BF16, KR, VR>;
