@@ -107,32 +107,34 @@ __device__ __forceinline__ void store_zero_row(uint16_t* dst) {
 }  // namespace
 
 // ------------------------------------------------------------------------------------------
-// kernel 0: -scale D = -scale rowsum(dO o O) and -L log2(e), one warp per (padded) query row
+// kernel 0: -scale D = -scale rowsum(dO o O) and -L log2(e), d / 8 lanes per (padded) query row
 // ------------------------------------------------------------------------------------------
 template <int D, bool BF16>
 __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
                                     float* lse2, float* dvec, int N_q, int nqp, long long rows,
                                     float scale) {
-  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= rows) return;
-  const long long bh = w / nqp;
-  const int i = static_cast<int>(w - bh * nqp);
+  // D / 8 lanes per row, 16-byte loads of O and dO; 32 / (D / 8) rows per warp
+  constexpr int kLanes = D / 8;
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kLanes;
+  const int lane = threadIdx.x % kLanes;
+  const bool in = w < rows;
+  const long long bh = in ? w / nqp : 0;
+  const int i = in ? static_cast<int>(w - bh * nqp) : 0;
   float acc = 0.0f;
-  if (i < N_q) {
-    const size_t base = (static_cast<size_t>(bh) * N_q + i) * D;
-    const uint32_t* o2 = reinterpret_cast<const uint32_t*>(o + base);
-    const uint32_t* d2 = reinterpret_cast<const uint32_t*>(dout + base);
+  if (in && i < N_q) {
+    const size_t base = (static_cast<size_t>(bh) * N_q + i) * D + lane * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int c = lane; c < D / 2; c += 32) {
-      const uint32_t a = o2[c], b = d2[c];
-      acc = fmaf(half_to_f32<BF16>(a & 0xffffu), half_to_f32<BF16>(b & 0xffffu), acc);
-      acc = fmaf(half_to_f32<BF16>(a >> 16), half_to_f32<BF16>(b >> 16), acc);
+    for (int c = 0; c < 4; ++c) {
+      acc = fmaf(half_to_f32<BF16>(av[c] & 0xffffu), half_to_f32<BF16>(bv[c] & 0xffffu), acc);
+      acc = fmaf(half_to_f32<BF16>(av[c] >> 16), half_to_f32<BF16>(bv[c] >> 16), acc);
     }
   }
 #pragma unroll
-  for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-  if (lane == 0) {
+  for (int sh = kLanes / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (in && lane == 0) {
     // stored negated (and D times the scale), so that the elementwise steps are single FMAs:
     // s * scale log2(e) + (-L log2(e)) and dP * scale + (-scale D)
     dvec[w] = (i < N_q) ? -scale * acc : 0.0f;
@@ -143,50 +145,65 @@ __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, con
 // ------------------------------------------------------------------------------------------
 // kernel 1: dK, dV of one 128-key tile
 // ------------------------------------------------------------------------------------------
-// Tensor memory: S^T 0-127, dP^T 128-255, dV 256-(256+d), dK after it.  The two elementwise
-// warpgroups split the 128 queries of a tile (warpgroup w: queries 64w .. 64w+63); each writes
-// P^T and then dS^T as 16-bit pairs into the S^T columns it has already read (P^T of warpgroup
-// w at columns 64w .. 64w+31, dS^T at 64w+32 .. 64w+63), so that dP^T is free as soon as it has
-// been read and the next tile's dP^T runs during this tile's dS^T step.
+// The query tiles stream through a ring of shared-memory stages of 64 queries (Q, dO, and their
+// L log2(e) and D), taken one stage per step: S^T and dP^T (128 keys x 64 queries) are
+// double-buffered in tensor memory, and elementwise warpgroup w takes the steps of buffer w, so
+// that the MMAs of one step run while the elementwise step of the other is computed.  Tensor
+// memory: S^T[2] 0-127, dP^T[2] 128-255, dV 256-(256+d), dK after it; P^T and dS^T go back as
+// 16-bit pairs over the first 32 columns of the buffers they came from.
+constexpr int kStepQ = 64;  // queries per step of the dK/dV kernel
+
 template <int D, int QS>
 struct KvLayout {
-  static constexpr uint32_t kTile = kBT * D * 2;
-  static constexpr uint32_t kStage = 2 * kTile + 1024;  // Q, dO, then L log2(e) and D [128] each
+  static constexpr uint32_t kTile = kBT * D * 2;             // K or V: 128 rows
+  static constexpr uint32_t kHalf = kStepQ * D * 2;          // Q or dO: 64 rows
+  static constexpr uint32_t kHalfSub = kStepQ * 128;         // one 64-column sub-tile of it
+  static constexpr uint32_t kStage = (2 * kHalf + 512 + 1023) / 1024 * 1024;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
-  // kv_full, st_full[QS], st_empty[QS], s_full, dp_full, p_ready, dp_free, ds_ready, drain
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 6;
+  // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], pds_ready[2], drain
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 7;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tile alignment");
+  static_assert(kTile % 1024 == 0 && kHalf % 1024 == 0, "tile alignment");
   static_assert(kBytes <= 232448, "shared memory per block");
 };
 
-// K-major A x K-major B^T, both 128 rows x D (the two 64-column halves of d are separate swizzled
-// sub-tiles): D[128 x 128] (+)= A B^T.
+// K-major A (128 rows x D, 64-column sub-tiles a_sub bytes apart) x K-major B^T (N rows x D,
+// sub-tiles b_sub apart): D[128 x N] = A B^T.
 template <int D>
-__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                              uint32_t idesc) {
+__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t a_sub,
+                                              uint32_t b_smem, uint32_t b_sub, uint32_t idesc) {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-    mma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
-           idesc, kk > 0 ? 1u : 0u);
-  }
+  for (int kk = 0; kk < D / 16; ++kk)
+    mma_ss(d_tmem, make_sdesc_sw128(a_smem + (kk >> 2) * a_sub + (kk & 3) * 32, 16, 1024),
+           make_sdesc_sw128(b_smem + (kk >> 2) * b_sub + (kk & 3) * 32, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
 }
 
-// A [128 x 128] in tensor memory as 16-bit pairs, the first 64 of its K elements at columns
-// a_tmem .. +31 and the second 64 at a_tmem + 64 .. +95 (one half per elementwise warpgroup),
-// times B [128 rows x D] in shared memory read MN-major: D[128 x D] (+)= A B.
-__device__ __forceinline__ void mma_split_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                               uint32_t idesc, bool accumulate) {
+// The same from the descriptors of the operands' first K step: a descriptor's start address
+// field counts 16-byte units, so a later K step's descriptor is the first one plus a constant
+// (the issuing thread builds two descriptors per product instead of two per MMA).
+template <int D, uint32_t A_SUB, uint32_t B_SUB>
+__device__ __forceinline__ void mma_rows_rows_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc) {
 #pragma unroll
-  for (int kk = 0; kk < kBT / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
-           make_sdesc_sw128(b_smem + kk * 16 * 128, kSub, 1024), idesc,
+  for (int kk = 0; kk < D / 16; ++kk)
+    mma_ss(d_tmem, a_desc + (((kk >> 2) * A_SUB + (kk & 3) * 32) >> 4),
+           b_desc + (((kk >> 2) * B_SUB + (kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
+}
+
+// A [128 x K] in tensor memory as 16-bit pairs (K / 2 columns from a_tmem) times B [K rows x D]
+// in shared memory read MN-major, from the descriptor of its first 16 rows: D[128 x D] (+)= A B.
+template <int K>
+__device__ __forceinline__ void mma_tmem_rows_d(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < K / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + ((kk * 16 * 128) >> 4), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -205,12 +222,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_kv = bars;
 #define ST_FULL(s) (bars + 8u * (1 + (s)))
 #define ST_EMPTY(s) (bars + 8u * (1 + QS + (s)))
-  const uint32_t bar_s = bars + 8u * (1 + 2 * QS);  // S^T_i written (MMA commit)
-  const uint32_t bar_dp = bar_s + 8;                 // dP^T_i written (MMA commit)
-  const uint32_t bar_p = bar_s + 16;                 // P^T_i stored (256 arrivals)
-  const uint32_t bar_dpfree = bar_s + 24;            // dP^T_i read (256 arrivals)
-  const uint32_t bar_ds = bar_s + 32;                // dS^T_i stored (256 arrivals)
-  const uint32_t bar_drain = bar_s + 40;
+  const uint32_t bar_b = bars + 8u * (1 + 2 * QS);
+#define S_FULL(b) (bar_b + 8u * (b))           // S^T of buffer b written (MMA commit)
+#define DP_FULL(b) (bar_b + 8u * (2 + (b)))     // dP^T of buffer b written (MMA commit)
+#define PDS_READY(b) (bar_b + 8u * (4 + (b)))   // P^T and dS^T of buffer b stored (128 arrivals)
+  const uint32_t bar_drain = bar_b + 8u * 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -232,6 +248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   const int nq_per = p.n_qtiles - qt_lo;  // query tiles per query head
   const int n = nq_per > 0 ? p.G * nq_per : 0;
+  const int n_steps = 2 * n;              // two 64-query steps per query tile
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -239,11 +256,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(ST_FULL(s), 1);
       mbar_init(ST_EMPTY(s), 1);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_dp, 1);
-    mbar_init(bar_p, 2 * kEwThreads);
-    mbar_init(bar_dpfree, 2 * kEwThreads);
-    mbar_init(bar_ds, 2 * kEwThreads);
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(S_FULL(bb), 1);
+      mbar_init(DP_FULL(bb), 1);
+      mbar_init(PDS_READY(bb), kEwThreads);
+    }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -270,22 +287,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(base + L::kV + sub * kSub, &tm_v, bar_kv, sub * 64, kt * kBT, bkv);
       }
       int issued = 0;
-      for (int i = 0; i < n; ++i) {
+      for (int i = 0; i < n_steps; ++i) {
         const int s = i % QS;
         if (i >= QS && !wait_bounded(ST_EMPTY(s), ((i / QS) - 1) & 1, abort_flag, p.status)) break;
-        const int g = i / nq_per;
-        const int qt = qt_lo + i % nq_per;
+        const int tile = i >> 1;
+        const int g = tile / nq_per;
+        const int q0 = (qt_lo + tile % nq_per) * kBT + (i & 1) * kStepQ;
         const int bhq = b * p.Hq + hk * p.G + g;
         const uint32_t st = base + L::kStages + s * L::kStage;
-        mbar_arrive_expect_tx(ST_FULL(s), 2 * L::kTile + 1024);
+        mbar_arrive_expect_tx(ST_FULL(s), 2 * L::kHalf + 512);
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub) {
-          tma_load_3d(st + sub * kSub, &tm_q, ST_FULL(s), sub * 64, qt * kBT, bhq);
-          tma_load_3d(st + L::kTile + sub * kSub, &tm_do, ST_FULL(s), sub * 64, qt * kBT, bhq);
+          tma_load_3d(st + sub * L::kHalfSub, &tm_q, ST_FULL(s), sub * 64, q0, bhq);
+          tma_load_3d(st + L::kHalf + sub * L::kHalfSub, &tm_do, ST_FULL(s), sub * 64, q0, bhq);
         }
-        const size_t vec = static_cast<size_t>(bhq) * p.nqp + static_cast<size_t>(qt) * kBT;
-        bulk_load(st + 2 * L::kTile, p.lse2 + vec, kBT * 4, ST_FULL(s));
-        bulk_load(st + 2 * L::kTile + 512, p.dvec + vec, kBT * 4, ST_FULL(s));
+        const size_t vec = static_cast<size_t>(bhq) * p.nqp + static_cast<size_t>(q0);
+        bulk_load(st + 2 * L::kHalf, p.lse2 + vec, kStepQ * 4, ST_FULL(s));
+        bulk_load(st + 2 * L::kHalf + 256, p.dvec + vec, kStepQ * 4, ST_FULL(s));
         issued = i + 1;
       }
       wait_bounded(bar_kv, 0, nullptr, p.status, kBwdDrainNs);
@@ -295,45 +313,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBT, kStepQ, false);
       constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
-      // Per query tile i: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; dV += P^T_i dO_i once P^T_i is
-      // stored; dK += dS^T_i Q_i once dS^T_i is stored; then dP^T_{i+1} (dP^T_i has been read)
-      // and S^T_{i+1}, which overwrites the columns dV_i and dK_i read (the MMAs of one thread
-      // run in issue order).
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % QS;
+      // Step i in buffer i % 2: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; once P^T_i and dS^T_i
+      // are stored, dV += P^T_i dO_i and dK += dS^T_i Q_i; then step i + 2's products into the
+      // same buffer (the MMAs of one thread run in issue order).  The elementwise warpgroups
+      // run ahead of the issuer, so the waits below are normally satisfied already: one wait
+      // per step, and descriptors built once per product, keep the issuing thread's work
+      // between MMAs small (the tensor pipe queues only one or two of them).
+      const uint64_t dk_desc = make_sdesc_sw128(base + L::kK, 16, 1024);
+      const uint64_t dv_desc = make_sdesc_sw128(base + L::kV, 16, 1024);
+      auto issue_sdp = [&](int i) -> bool {
+        const int s = i % QS, bb = i & 1;
         if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + L::kColS, base + L::kK, base + L::kStages + s * L::kStage, idesc_rr);
-        mma_commit(bar_s);
-        return true;
-      };
-      auto issue_dp = [&](int i) -> bool {
-        const int s = i % QS;
-        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        mma_rows_rows<D>(tmem + L::kColDP, base + L::kV,
-                         base + L::kStages + s * L::kStage + L::kTile, idesc_rr);
-        mma_commit(bar_dp);
-        return true;
-      };
-      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_s(0) && issue_dp(0);
-      for (int i = 0; ok && i < n; ++i) {
-        const int s = i % QS;
         const uint32_t st = base + L::kStages + s * L::kStage;
-        if (!wait_bounded(bar_p, i & 1, abort_flag, p.status)) break;
+        mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColS + bb * kStepQ, dk_desc,
+                                               make_sdesc_sw128(st, 16, 1024), idesc_s);
+        mma_commit(S_FULL(bb));
+        mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColDP + bb * kStepQ, dv_desc,
+                                               make_sdesc_sw128(st + L::kHalf, 16, 1024), idesc_s);
+        mma_commit(DP_FULL(bb));
+        return true;
+      };
+      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_sdp(0) &&
+                (n_steps < 2 || issue_sdp(1));
+      for (int i = 0; ok && i < n_steps; ++i) {
+        const int s = i % QS, bb = i & 1;
+        const uint32_t st = base + L::kStages + s * L::kStage;
+        if (!wait_bounded(PDS_READY(bb), (i >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_split_rows(tmem + L::kColDV, tmem + L::kColS, st + L::kTile, idesc_acc, i > 0);  // dV
-        if (!wait_bounded(bar_ds, i & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        mma_split_rows(tmem + L::kColDK, tmem + L::kColS + 32, st, idesc_acc, i > 0);  // dK
+        mma_tmem_rows_d<kStepQ>(tmem + L::kColDV, tmem + L::kColS + bb * kStepQ,
+                                make_sdesc_sw128(st + L::kHalf, L::kHalfSub, 1024), idesc_acc,
+                                i > 0);  // dV += P^T dO
+        mma_tmem_rows_d<kStepQ>(tmem + L::kColDK, tmem + L::kColDP + bb * kStepQ,
+                                make_sdesc_sw128(st, L::kHalfSub, 1024), idesc_acc,
+                                i > 0);  // dK += dS^T Q
         mma_commit(ST_EMPTY(s));
-        // dP^T_{i+1} then S^T_{i+1}: as late as the elementwise step allows (it needs both
-        // only after dS^T_i), which gives the load of stage i + 1 (freed by dK_{i-1}) time
-        if (!wait_bounded(bar_dpfree, i & 1, abort_flag, p.status)) break;
-        if (i + 1 < n && !issue_dp(i + 1)) break;
-        if (i + 1 < n) ok = issue_s(i + 1);
+        if (i + 2 < n_steps) ok = issue_sdp(i + 2);
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -341,38 +358,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise (thread = key)
-    // Warpgroup w takes queries c0 = 64w .. c0+63 of every query tile; thread r owns key row r
-    // (warp % 4 is its tensor-memory lane quarter).
+    // Warpgroup w takes the steps of buffer w; thread r owns key row r (warp % 4 is its
+    // tensor-memory lane quarter).
     const int wg = warp >> 2;
-    const int c0 = wg * 64;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int kr = kt * kBT + r;  // this thread's key
     const uint32_t row_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.sl2, scale = p.scale;
     const int q_first_visible = kr - off;  // the smallest query row that sees this key
+    const uint32_t s_col = L::kColS + wg * kStepQ, dp_col = L::kColDP + wg * kStepQ;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
+    for (int i = wg; i < n_steps; i += 2) {
       const int s = i % QS;
-      const int qt = qt_lo + i % nq_per;
+      const int tile = i >> 1;
+      const int q0 = (qt_lo + tile % nq_per) * kBT + (i & 1) * kStepQ;
       const float* lv = reinterpret_cast<const float*>(gbase + L::kStages + s * L::kStage +
-                                                       2 * L::kTile) + c0;
-      const float* dvv = lv + kBT;
-      const int q0 = qt * kBT + c0;
-      if (!ew_wait(bar_s, i & 1, abort_flag, p.status)) {
+                                                       2 * L::kHalf);
+      const float* dvv = lv + kStepQ;
+      if (!ew_wait(S_FULL(wg), (i >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // P^T row of this key over the warpgroup's 64 queries, kept in registers for dS^T:
+      // P^T row of this key over the step's 64 queries, kept in registers for dS^T:
       // p = 2^(s scale log2(e) - L log2(e)), one packed FMA per pair; the causal test only
       // where some query of the 64 precedes this key
-      float pv[64];
-      uint32_t pp[32];
+      float pv[kStepQ];
+      uint32_t pp[kStepQ / 2];
       {
         uint32_t sv[2][32];
-        tmem_ld32(row_tmem + L::kColS + c0, sv[0]);
-        tmem_ld32(row_tmem + L::kColS + c0 + 32, sv[1]);
+        tmem_ld32(row_tmem + s_col, sv[0]);
+        tmem_ld32(row_tmem + s_col + 32, sv[1]);
         tmem_wait_ld();
         const bool full = !p.causal || q0 >= q_first_visible;
         const bool all_full = __all_sync(0xffffffffu, full);
@@ -401,23 +418,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pp[(col >> 1) + 1] = pack2<BF16>(pv[col + 2], pv[col + 3]);
           }
       }
-      tmem_st32(row_tmem + L::kColS + c0, pp);  // P^T over the S^T columns already read
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
-      if (!ew_wait(bar_dp, i & 1, abort_flag, p.status)) {
+      tmem_st32(row_tmem + s_col, pp);  // P^T over the S^T columns already read
+      if (!ew_wait(DP_FULL(wg), (i >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t dpv[2][32];
-      tmem_ld32(row_tmem + L::kColDP + c0, dpv[0]);
-      tmem_ld32(row_tmem + L::kColDP + c0 + 32, dpv[1]);
+      tmem_ld32(row_tmem + dp_col, dpv[0]);
+      tmem_ld32(row_tmem + dp_col + 32, dpv[1]);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_dpfree);  // dP^T_{i+1} may overwrite
       // dS^T = P^T o (dP^T - D) scale = P^T o (dP^T scale + (-scale D)): two packed FMAs a pair
-      uint32_t dd[32];
+      uint32_t dd[kStepQ / 2];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -433,10 +445,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dd[col >> 1] = pack2<BF16>(g0, g1);
           dd[(col >> 1) + 1] = pack2<BF16>(g2, g3);
         }
-      tmem_st32(row_tmem + L::kColS + c0 + 32, dd);  // dS^T beside this warpgroup's P^T
-      tmem_wait_st();
+      tmem_st32(row_tmem + dp_col, dd);  // dS^T over the dP^T columns already read
+      tmem_wait_st();  // both stores (P^T and dS^T) have landed
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      mbar_arrive(PDS_READY(wg));
     }
     // epilogue: warpgroup 0 stores dV, warpgroup 1 dK, once the last MMA has finished
     if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
@@ -453,6 +465,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 #undef ST_FULL
 #undef ST_EMPTY
+#undef S_FULL
+#undef DP_FULL
+#undef PDS_READY
   tc_fence_before();
   __syncthreads();
   if (warp == kBwdIssuerWarp) {
@@ -468,6 +483,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // warpgroups split the 128 keys of a tile (warpgroup w: keys 64w .. 64w+63); each keeps its P
 // in registers and writes dS as 16-bit pairs over the S columns it has read (64w .. 64w+31 of
 // the tile's S buffer), so that dP is free as soon as it has been read.
+// A [128 x 128] in tensor memory as 16-bit pairs, the first 64 of its K elements at columns
+// a_tmem .. +31 and the second 64 at a_tmem + 64 .. +95 (one half per elementwise warpgroup),
+// times B [128 rows x D] in shared memory read MN-major: D[128 x D] (+)= A B.
+__device__ __forceinline__ void mma_split_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                               uint32_t idesc, bool accumulate) {
+  const uint64_t b_desc = make_sdesc_sw128(b_smem, kSub, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kBT / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b_desc + ((kk * 16 * 128) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
 template <int D, int KR, int VR>
 struct QLayout {
   static constexpr uint32_t kTile = kBT * D * 2;
@@ -594,12 +621,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
       // S_t = Q K_t^T into buffer t % 2 (next written by S_{t+2}, issued after dQ_t, which
       // reads dS_t there); dP_t = dO V_t^T once dP_{t-1} has been read; dQ += dS_t K_t.
+      const uint64_t q_desc = make_sdesc_sw128(base + L::kQ, 16, 1024);
+      const uint64_t do_desc = make_sdesc_sw128(base + L::kDO, 16, 1024);
       auto issue_s = [&](int t) -> bool {
         const int s = t % KR;
         if (!wait_bounded(K_FULL(s), (t / KR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + L::kColS + (t & 1) * 128, base + L::kQ, base + L::kK + s * L::kTile,
-                         idesc_rr);
+        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColS + (t & 1) * 128, q_desc,
+                                       make_sdesc_sw128(base + L::kK + s * L::kTile, 16, 1024),
+                                       idesc_rr);
         mma_commit(bar_sfull + 8u * (t & 1));
         return true;
       };
@@ -607,7 +637,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int s = t % VR;
         if (!wait_bounded(V_FULL(s), (t / VR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + L::kColDP, base + L::kDO, base + L::kV + s * L::kTile, idesc_rr);
+        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColDP, do_desc,
+                                       make_sdesc_sw128(base + L::kV + s * L::kTile, 16, 1024),
+                                       idesc_rr);
         mma_commit(bar_dp);
         mma_commit(V_EMPTY(s));
         return true;
@@ -739,7 +771,7 @@ size_t bwd_workspace_bytes(int B, int Hq, int N_q) {
 
 template <int D, bool BF16>
 static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
-  constexpr int QS = (D == 128) ? 2 : 4;  // query-tile stages of the dK/dV kernel
+  constexpr int QS = (D == 128) ? 4 : 6;  // 64-query stages of the dK/dV kernel
   constexpr int KR = (D == 128) ? 3 : 4;  // K slots of the dQ kernel
   constexpr int VR = (D == 128) ? 2 : 4;  // V slots of the dQ kernel
   using LK = KvLayout<D, QS>;
@@ -748,6 +780,10 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t bhk = static_cast<uint64_t>(a.B) * a.Hkv;
   const uint64_t rb = static_cast<uint64_t>(D) * 2;
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq64, tdo64;  // 64-row boxes: the stages of the dK/dV kernel
+  if (!make_tmap_3d(&tq64, a.q, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kStepQ, 1) ||
+      !make_tmap_3d(&tdo64, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kStepQ, 1))
+    return -5;
   if (!make_tmap_3d(&tq, a.q, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
       !make_tmap_3d(&tdo, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
       !make_tmap_3d(&tk, a.k, BF16, D, a.N_kv, bhk, rb, rb * a.N_kv, 64, kBT, 1) ||
@@ -779,7 +815,7 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.sl2 = a.scale * 1.4426950408889634f;
   const long long rows = static_cast<long long>(bhq) * nqp;
-  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+  attn_bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse,
       const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), a.N_q, nqp, rows, a.scale);
   if (cudaGetLastError() != cudaSuccess) return -5;
@@ -791,7 +827,7 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t kv_blocks = bhk * p.n_kvtiles;
   const uint64_t q_blocks = bhq * n_qtiles;
   if (kv_blocks > 0x7fffffffull || q_blocks > 0x7fffffffull) return -2;
-  kkv<<<static_cast<unsigned>(kv_blocks), kBwdThreads, LK::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  kkv<<<static_cast<unsigned>(kv_blocks), kBwdThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p);
   if (cudaGetLastError() != cudaSuccess) return -5;
   kq<<<static_cast<unsigned>(q_blocks), kBwdThreads, LQ::kBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
