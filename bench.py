@@ -281,17 +281,24 @@ def run_ours(args):
                                 dcfg.Hkv, dcfg.d, dcfg.dtype, dcfg.seed, lengths_override=lens)
     do_pre = args.only in ("both", "prefill")
     do_dec = args.only in ("both", "decode")
-    q, k, v = pcfg.device_inputs(device)
-    o = torch.empty_like(q)
-    lse = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), device=device, dtype=torch.float32)
+    # each path's tensors only when it runs (a one-path run, e.g. under a profiler, then holds
+    # only its own inputs)
+    q = k = v = o = lse = None
+    if do_pre:
+        q, k, v = pcfg.device_inputs(device)
+        o = torch.empty_like(q)
+        lse = torch.empty((pcfg.B, pcfg.Hq, pcfg.N_q), device=device, dtype=torch.float32)
     lengths = dcfg.lengths()
-    cu = torch.from_numpy(syn.cu_seqlens(lengths)).to(device)
     max_len = int(lengths.max())
-    dq, dk, dv = dcfg.device_inputs(device)
-    do = torch.empty_like(dq)
-    dl = torch.empty((dcfg.B, dcfg.Hq), device=device, dtype=torch.float32)
-    ws = torch.empty(attn.attn_decode_workspace_bytes(dcfg.B, dcfg.Hq, max_len, dcfg.split, dcfg.d),
-                     device=device, dtype=torch.uint8)
+    cu = dq = dk = dv = do = dl = ws = None
+    if do_dec:
+        cu = torch.from_numpy(syn.cu_seqlens(lengths)).to(device)
+        dq, dk, dv = dcfg.device_inputs(device)
+        do = torch.empty_like(dq)
+        dl = torch.empty((dcfg.B, dcfg.Hq), device=device, dtype=torch.float32)
+        ws = torch.empty(attn.attn_decode_workspace_bytes(dcfg.B, dcfg.Hq, max_len, dcfg.split,
+                                                          dcfg.d),
+                         device=device, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
     def prefill():
@@ -340,7 +347,8 @@ def run_ours(args):
 
     flops = pcfg.flops()
     kv_bytes = dcfg.kv_bytes()
-    dec_bytes = kv_bytes + 2 * dq.numel() * 2 + dl.numel() * 4
+    # K and V read, q read and o written (2 B each), LSE written (4 B)
+    dec_bytes = kv_bytes + 2 * (dcfg.B * dcfg.Hq * dcfg.d) * 2 + dcfg.B * dcfg.Hq * 4
     tiny = 1e-9
     value = flops * args.steps * world / (max(pre_ms_max, tiny) / 1e3) / 1e12 if do_pre else None
     dec_gbs = dec_bytes * args.steps * world / (max(dec_ms_max, tiny) / 1e3) / 1e9 if do_dec else None
@@ -398,7 +406,9 @@ def run_ours(args):
             "frac_of_spec_2250": round(ach_t / 2250.0, 4),
             "traffic": profiled_traffic("attn_fwd_kernel", FWD_SOURCES),
             # compulsory bytes of one launch: Q, K, V read, O written (2 B each), LSE (4 B)
-            "algorithmic_bytes": int((2 * q.numel() + 2 * k.numel()) * 2 + lse.numel() * 4),
+            "algorithmic_bytes": int((2 * pcfg.B * pcfg.Hq * pcfg.N_q * pcfg.d
+                                      + 2 * pcfg.B * pcfg.Hkv * pcfg.N_kv * pcfg.d) * 2
+                                     + pcfg.B * pcfg.Hq * pcfg.N_q * 4),
         },
         "decode": {
             "value": round(dec_gbs, 1) if dec_gbs is not None else None,

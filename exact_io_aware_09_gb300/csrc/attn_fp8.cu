@@ -26,13 +26,13 @@ constexpr int kT = 128;        // rows of a tile
 constexpr int kPrepThreads = 256;
 constexpr int kPrepWarps = kPrepThreads / 32;
 
-// Four consecutive 16-bit values (8 bytes) as floats.
+// Eight consecutive 16-bit values (16 bytes) as floats.
 template <bool BF16>
-__device__ __forceinline__ void load4(const uint16_t* p, float v[4]) {
-  const uint2 w = *reinterpret_cast<const uint2*>(p);
-  const uint32_t h[2] = {w.x, w.y};
+__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t h[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 4; ++i) {
     if constexpr (BF16) {
       v[2 * i] = __uint_as_float(h[i] << 16);
       v[2 * i + 1] = __uint_as_float(h[i] & 0xffff0000u);
@@ -48,10 +48,9 @@ __device__ __forceinline__ void load4(const uint16_t* p, float v[4]) {
   }
 }
 
-// Eight consecutive 16-bit values (16 bytes) as floats.
+// Eight 16-bit values already loaded (16 bytes) as floats.
 template <bool BF16>
-__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void load8_words(const uint4 w, float v[8]) {
   const uint32_t h[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -87,19 +86,21 @@ __device__ __forceinline__ float scale_of(float amax) {
 }  // namespace
 
 // One block per (plane, 128-row tile) of Q or of K (blocks [0, q_blocks) take Q): rotate
-// (optional), tile amax, quantise.  A warp takes one row at a time, lane l holding channels
-// 4l .. 4l+3, so that loads (8 bytes a lane) and code stores (4 bytes a lane) are coalesced.
-// Butterfly stages h = 1, 2 are inside a lane; stage h = 4m pairs lane l with lane l ^ m: the
-// lane without bit m keeps a + b, the other b' = a - b, the same fp32 operations in the same
-// order as the plain loop over j.
+// (optional), tile amax, quantise.  The tile passes through shared memory twice so that global
+// memory sees only coalesced 16-byte accesses: the 16-bit rows are loaded by consecutive threads,
+// then thread r takes row r whole (padded rows, conflict-free 16-byte reads) and runs every
+// butterfly stage in registers, in the plain order (h = 1, 2, ..., d/2); its E4M3 codes go back
+// through shared memory and out as coalesced rows.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kT)
     fp8_rotate_quantize_kernel(const uint16_t* xq, const uint16_t* xk, const int8_t* signs,
                                float inv_sqrt_d, uint8_t* cq, uint8_t* ck, float* sq, float* sk,
                                int Nq, int Nk, int nqt, int nkt, int q_blocks) {
-  static_assert(D == 128, "one 4-channel slice per lane");
-  constexpr int kRows = kT / kPrepWarps;  // rows per warp
-  __shared__ float red[kPrepWarps];
+  static_assert(D == 128, "one row of 128 channels per thread");
+  constexpr int kPitch = D * 2 + 16;  // bytes per staged 16-bit row (16-byte reads conflict-free)
+  constexpr int kCodePitch = D + 16;  // bytes per staged code row
+  __shared__ __align__(16) uint8_t stage[kT * kPitch];
+  __shared__ float red[kT / 32];
   const bool is_q = static_cast<int>(blockIdx.x) < q_blocks;
   const int b = is_q ? blockIdx.x : blockIdx.x - q_blocks;
   const int n_tiles = is_q ? nqt : nkt;
@@ -107,69 +108,81 @@ __global__ void __launch_bounds__(kPrepThreads)
   const uint16_t* x = is_q ? xq : xk;
   uint8_t* codes = is_q ? cq : ck;
   const int plane = b / n_tiles, tile = b % n_tiles;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float sg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+  const int rows = min(kT, N - tile * kT);
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (static_cast<size_t>(plane) * N +
+                                                               static_cast<size_t>(tile) * kT) * D);
+  // 1. coalesced load of the tile's rows (rows past the end read as zeros)
+  constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of a row
+#pragma unroll 4
+  for (int u = threadIdx.x; u < kT * kChunks; u += kT) {
+    const int row = u / kChunks, c = u % kChunks;
+    const uint4 w = row < rows ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D * 2 + c * 16)
+                               : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(stage + row * kPitch + c * 16) = w;
+  }
+  // signs as four 32-bit masks (bit c set: channel c is negated), the same in every thread
+  uint32_t neg[D / 32] = {};
+  if (signs) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) neg[q] = __ballot_sync(0xffffffffu, signs[q * 32 + lane] < 0);
+  }
+  __syncthreads();
+  // 2. thread r: row r
+  float v[D];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + threadIdx.x * kPitch + c * 16);
+    float f[8];
+    load8_words<BF16>(w, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[c * 8 + e] = f[e];
+  }
   if (signs) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sg[e] = signs[4 * lane + e] < 0 ? -1.0f : 1.0f;
-  }
-  float v[kRows][4];
+    for (int c = 0; c < D; ++c)
+      v[c] = __int_as_float(__float_as_int(v[c]) ^ (((neg[c >> 5] >> (c & 31)) & 1u) << 31));
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int row = tile * kT + warp + i * kPrepWarps;
-    if (row < N) {
-      load4<BF16>(x + (static_cast<size_t>(plane) * N + row) * D + 4 * lane, v[i]);
-    } else {
+    for (int h = 1; h < D; h <<= 1)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[i][e] = 0.0f;
-    }
+      for (int j = 0; j < D; ++j)
+        if ((j & h) == 0) {
+          const float a = v[j], c = v[j + h];
+          v[j] = a + c;
+          v[j + h] = a - c;
+        }
+#pragma unroll
+    for (int c = 0; c < D; ++c) v[c] = v[c] * inv_sqrt_d;
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    if (signs) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[i][e] = sg[e] < 0.0f ? -v[i][e] : v[i][e];
-      // h = 1: (0, 1), (2, 3); h = 2: (0, 2), (1, 3)
-      float a = v[i][0], c = v[i][1];
-      v[i][0] = a + c;
-      v[i][1] = a - c;
-      a = v[i][2];
-      c = v[i][3];
-      v[i][2] = a + c;
-      v[i][3] = a - c;
-      a = v[i][0];
-      c = v[i][2];
-      v[i][0] = a + c;
-      v[i][2] = a - c;
-      a = v[i][1];
-      c = v[i][3];
-      v[i][1] = a + c;
-      v[i][3] = a - c;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float other = __shfl_xor_sync(0xffffffffu, v[i][e], m);
-          v[i][e] = upper ? other - v[i][e] : v[i][e] + other;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[i][e] = v[i][e] * inv_sqrt_d;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
-  }
+  for (int c = 0; c < D; ++c) amax = fmaxf(amax, fabsf(v[c]));
+  // 3. tile amax, scale, codes (the block reduction's barriers also end every read of the stage)
   const float scale = scale_of(block_max(amax, red));
   if (threadIdx.x == 0) (is_q ? sq : sk)[b] = scale;
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int row = tile * kT + warp + i * kPrepWarps;
-    if (row < N)
-      *reinterpret_cast<uint32_t*>(codes + (static_cast<size_t>(plane) * N + row) * D + 4 * lane) =
-          pack4_e4m3(__fdiv_rn(v[i][0], scale), __fdiv_rn(v[i][1], scale),
-                     __fdiv_rn(v[i][2], scale), __fdiv_rn(v[i][3], scale));
+  for (int c = 0; c < D; c += 16) {
+    uint4 w;
+    w.x = pack4_e4m3(__fdiv_rn(v[c + 0], scale), __fdiv_rn(v[c + 1], scale),
+                     __fdiv_rn(v[c + 2], scale), __fdiv_rn(v[c + 3], scale));
+    w.y = pack4_e4m3(__fdiv_rn(v[c + 4], scale), __fdiv_rn(v[c + 5], scale),
+                     __fdiv_rn(v[c + 6], scale), __fdiv_rn(v[c + 7], scale));
+    w.z = pack4_e4m3(__fdiv_rn(v[c + 8], scale), __fdiv_rn(v[c + 9], scale),
+                     __fdiv_rn(v[c + 10], scale), __fdiv_rn(v[c + 11], scale));
+    w.w = pack4_e4m3(__fdiv_rn(v[c + 12], scale), __fdiv_rn(v[c + 13], scale),
+                     __fdiv_rn(v[c + 14], scale), __fdiv_rn(v[c + 15], scale));
+    *reinterpret_cast<uint4*>(stage + threadIdx.x * kCodePitch + c) = w;
+  }
+  __syncthreads();
+  // 4. coalesced store of the code rows
+  uint8_t* dst = codes + (static_cast<size_t>(plane) * N + static_cast<size_t>(tile) * kT) * D;
+  constexpr int kCodeChunks = D / 16;
+#pragma unroll 4
+  for (int u = threadIdx.x; u < kT * kCodeChunks; u += kT) {
+    const int row = u / kCodeChunks, c = u % kCodeChunks;
+    if (row < rows)
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * D + c * 16) =
+          *reinterpret_cast<const uint4*>(stage + row * kCodePitch + c * 16);
   }
 }
 
@@ -289,7 +302,7 @@ int launch_attn_fwd_fp8(const FwdArgs& a, const int8_t* signs, void* workspace,
   auto run = [&](auto bf16_tag) -> int {
     constexpr bool BF = decltype(bf16_tag)::value;
     const uint16_t* v16 = static_cast<const uint16_t*>(a.v);
-    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kPrepThreads, 0, stream>>>(
+    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kT, 0, stream>>>(
         static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), signs, inv_sqrt_d,
         static_cast<uint8_t*>(const_cast<void*>(f.q8)), static_cast<uint8_t*>(const_cast<void*>(f.k8)),
         const_cast<float*>(f.q_scale), const_cast<float*>(f.k_scale), a.N_q, a.N_kv, nqt, nkt,
