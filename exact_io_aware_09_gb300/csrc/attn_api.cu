@@ -72,6 +72,22 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_4d(CUtensorMap* map, const void* base, bool bf16, const uint64_t dims[4],
+                  const uint64_t strides[3], const uint32_t box[4]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || dims[0] == 0 || dims[1] == 0 || dims[2] == 0 || dims[3] == 0) return false;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+         const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
                      uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                      uint32_t box1, uint32_t box2) {

@@ -21,7 +21,11 @@
 // cache in fixed-size non-contiguous blocks addressed through a block table, read by a split-KV
 // kernel): the same kernels with the producer reading each stage through the block table -- one
 // TMA box per stage when a page holds a whole 64-token stage, one box per page otherwise -- and
-// the sequence length taken from seqlens.
+// the sequence length taken from seqlens.  The cache is seen by TMA as a 4-D tensor {64
+// channels, token, channel half, head}, so that one box brings both 64-channel halves of its
+// rows: a stage holds R-row boxes (R = min(page size, 64); 64 for the packed cache) laid out
+// [box][half][R rows][128 B], and a 16-token page costs one TMA operation per tensor instead of
+// two.
 #include <mutex>
 
 #include "internal.h"
@@ -41,6 +45,7 @@ struct DecParams {
   const int32_t* block_table;  // [B, max_pages] (paged cache) or null
   const int32_t* seqlens;      // [B] (paged cache)
   int page_size, page_log2, max_pages, num_pages;
+  int box_log2;        // log2 of the rows of one TMA box: min(page_size, 64); 64 when packed
   float* ws_o;         // [B * Hq * max_splits, D]  normalised partial outputs
   float* ws_ml;        // [B * Hq * max_splits, 2]  (m in log2 units, l)
   int* status;
@@ -159,11 +164,8 @@ __global__ void __launch_bounds__(kDecThreads)
         const int tl = t0 + st * kDecTok;  // first token of the stage
         if (!p.block_table) {
           mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
-#pragma unroll
-          for (int hh = 0; hh < D / 64; ++hh) {
-            tma_load_3d(kbuf + hh * L::kHalf, &tm_k, FULL(s), hh * 64, hk, tl);
-            tma_load_3d(vbuf + hh * L::kHalf, &tm_v, FULL(s), hh * 64, hk, tl);
-          }
+          tma_load_4d(kbuf, &tm_k, FULL(s), 0, tl, 0, hk);
+          tma_load_4d(vbuf, &tm_v, FULL(s), 0, tl, 0, hk);
         } else {
           // Pages of this stage that hold tokens of the sequence: one when a page spans the
           // whole stage (its rows tl .. tl + 63 lie in one page), else 64 / page_size pages
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kDecThreads)
               const int r0 = page_row[(t >> p.page_log2) - first];
               if (r0 >= 0) {
                 phys[i] = r0 + (t & (p.page_size - 1));
-                bytes += 2u * (D / 64) * rows * 128u;
+                bytes += 2u * (D / 64) * rows * 128u;  // both tensors, both channel halves
               }
             }
           }
@@ -191,13 +193,9 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
           for (int i = 0; i < kDecTok / 16; ++i) {
             if (phys[i] < 0) continue;
-#pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh) {
-              tma_load_3d(kbuf + hh * L::kHalf + i * rows * 128, &tm_k, FULL(s), hh * 64, hk,
-                          phys[i]);
-              tma_load_3d(vbuf + hh * L::kHalf + i * rows * 128, &tm_v, FULL(s), hh * 64, hk,
-                          phys[i]);
-            }
+            const uint32_t box_off = static_cast<uint32_t>(i) * (D / 64) * rows * 128u;
+            tma_load_4d(kbuf + box_off, &tm_k, FULL(s), 0, phys[i], 0, hk);
+            tma_load_4d(vbuf + box_off, &tm_v, FULL(s), 0, phys[i], 0, hk);
           }
         }
         issued = st + 1;
@@ -229,6 +227,20 @@ __global__ void __launch_bounds__(kDecThreads)
   float o[D / 8][4];
 #pragma unroll
   for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  // Byte offset of (row, 64-channel half) in a stage of R = 2^box_log2-row boxes laid out
+  // [box][half][R rows][128 B]; the 128-byte swizzle's row phase is row % 8 in every layout.
+  const int bl2 = p.box_log2;
+  auto stage_off = [&](int row, int half) -> uint32_t {
+    return (static_cast<uint32_t>((row >> bl2) * (D / 64) + half) << (bl2 + 7)) +
+           (static_cast<uint32_t>(row & ((1 << bl2) - 1)) << 7);
+  };
+  // this lane's ldmatrix rows: K (scores) and V (the transposed P V operand)
+  uint32_t k_row[D / 64], v_row[D / 64];
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    k_row[h] = stage_off(warp * 16 + ((lane >> 4) << 3) + (lane & 7), h);
+    v_row[h] = stage_off(warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7), h);
+  }
 
   bool ok = true;
   for (int st = 0; st < n_stages; ++st) {
@@ -248,8 +260,8 @@ __global__ void __launch_bounds__(kDecThreads)
         for (int i = lane; i < (16 - valid) * (D / 8); i += 32) {
           const int rr = warp * 16 + valid + i / (D / 8);
           const int ch = i % (D / 8);
-          *reinterpret_cast<uint4*>(gbase + (vbuf - base) + (ch >> 3) * L::kHalf + sw128(rr, ch & 7)) =
-              make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(gbase + (vbuf - base) + stage_off(rr, ch >> 3) +
+                                    (((ch & 7) ^ (rr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
@@ -260,7 +272,7 @@ __global__ void __launch_bounds__(kDecThreads)
         const int chunk = ks * 2 + ((lane >> 3) & 1);
         const int key = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
         uint32_t b00, b01, b10, b11;
-        ldmatrix_x4(kbuf + (chunk >> 3) * L::kHalf + sw128(key, chunk & 7), b00, b01, b10, b11);
+        ldmatrix_x4(kbuf + k_row[chunk >> 3] + (((chunk & 7) ^ (key & 7)) << 4), b00, b01, b10, b11);
         mma_m16n8k16<BF16>(sc[0], qa[ks], b00, b01);
         mma_m16n8k16<BF16>(sc[1], qa[ks], b10, b11);
       }
@@ -315,7 +327,8 @@ __global__ void __launch_bounds__(kDecThreads)
         const int key = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
         const int chunk = nd2 * 2 + (lane >> 4);
         uint32_t v0, v1, v2, v3;
-        ldmatrix_x4_trans(vbuf + (chunk >> 3) * L::kHalf + sw128(key, chunk & 7), v0, v1, v2, v3);
+        ldmatrix_x4_trans(vbuf + v_row[chunk >> 3] + (((chunk & 7) ^ (key & 7)) << 4), v0, v1, v2,
+                          v3);
         mma_m16n8k16<BF16>(o[2 * nd2], pa, v0, v1);
         mma_m16n8k16<BF16>(o[2 * nd2 + 1], pa, v2, v3);
       }
@@ -439,9 +452,12 @@ static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
   const uint64_t tokens = paged ? static_cast<uint64_t>(a.num_pages) * a.page_size
                                 : static_cast<uint64_t>(a.kv_capacity);
   const uint32_t box_rows = paged ? static_cast<uint32_t>(min(a.page_size, kDecTok)) : kDecTok;
-  if (any_keys &&
-      (!make_tmap_3d(&tk, a.k_cache, BF16, D, a.Hkv, tokens, row, row * a.Hkv, 64, 1, box_rows) ||
-       !make_tmap_3d(&tv, a.v_cache, BF16, D, a.Hkv, tokens, row, row * a.Hkv, 64, 1, box_rows)))
+  // {64 channels, token, channel half, head}: one box = box_rows tokens x both halves of d
+  const uint64_t dims[4] = {64, tokens, D / 64, static_cast<uint64_t>(a.Hkv)};
+  const uint64_t strides[3] = {row * a.Hkv, 128, row};
+  const uint32_t box[4] = {64, box_rows, D / 64, 1};
+  if (any_keys && (!make_tmap_4d(&tk, a.k_cache, BF16, dims, strides, box) ||
+                   !make_tmap_4d(&tv, a.v_cache, BF16, dims, strides, box)))
     return -5;
   DecParams p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -451,6 +467,8 @@ static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
   p.page_size = a.page_size;
   p.page_log2 = 0;
   while (paged && (1 << p.page_log2) < a.page_size) ++p.page_log2;
+  p.box_log2 = 0;
+  while ((1u << p.box_log2) < box_rows) ++p.box_log2;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   const size_t parts = static_cast<size_t>(a.B) * a.Hq * (max_splits > 0 ? max_splits : 1);

@@ -14,6 +14,12 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, 
                   uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                   uint32_t box1, uint32_t box2);
 
+// A 4-D tiled TMA descriptor over a 16-bit tensor: dims {dim0 (innermost, elements), dim1,
+// dim2, dim3}, byte strides of dims 1-3 (in any order of size), box {box0 .. box3}, 128-byte
+// swizzle.  Returns false on failure.
+bool make_tmap_4d(CUtensorMap* map, const void* base, bool bf16, const uint64_t dims[4],
+                  const uint64_t strides[3], const uint32_t box[4]);
+
 // The same over a contiguous 8-bit tensor (E4M3 codes).
 bool make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
                      uint64_t dim2, uint64_t stride1, uint64_t stride2, uint32_t box0,
