@@ -479,43 +479,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ------------------------------------------------------------------------------------------
 // kernel 2: dQ of one 128-row query tile
 // ------------------------------------------------------------------------------------------
-// Tensor memory: S[2] 0-255 (double-buffered), dP 256-383, dQ 384-.  The two elementwise
-// warpgroups split the 128 keys of a tile (warpgroup w: keys 64w .. 64w+63); each keeps its P
-// in registers and writes dS as 16-bit pairs over the S columns it has read (64w .. 64w+31 of
-// the tile's S buffer), so that dP is free as soon as it has been read.
-// A [128 x 128] in tensor memory as 16-bit pairs, the first 64 of its K elements at columns
-// a_tmem .. +31 and the second 64 at a_tmem + 64 .. +95 (one half per elementwise warpgroup),
-// times B [128 rows x D] in shared memory read MN-major: D[128 x D] (+)= A B.
-__device__ __forceinline__ void mma_split_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                               uint32_t idesc, bool accumulate) {
-  const uint64_t b_desc = make_sdesc_sw128(b_smem, kSub, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kBT / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b_desc + ((kk * 16 * 128) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-}
-
+// Q stays in tensor memory as the A operand of S = Q K^T; dO (shared memory) is that of
+// dP = dO V^T.  Tensor memory: Q 0-63, S 64-191, dP 192-319, dS 320-383, dQ 384-.  The two
+// elementwise warpgroups split each tile's 128 keys and release S and dP as soon as they have
+// read them, and dS has its own buffer, so that the tensor pipe takes, per tile, S_{t+1} and
+// dP_{t+1} (issued while tile t's elementwise step runs) and then dQ += dS_t K_t: no product
+// waits for another tile's dS.
 template <int D, int KR, int VR>
 struct QLayout {
   static constexpr uint32_t kTile = kBT * D * 2;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kDO = kTile;
-  static constexpr uint32_t kK = 2 * kTile;          // K ring, KR slots
+  static constexpr uint32_t kDO = 0;                 // dO tile
+  static constexpr uint32_t kK = kTile;              // K ring, KR slots
   static constexpr uint32_t kV = kK + KR * kTile;    // V ring, VR slots
   static constexpr uint32_t kBar = kV + VR * kTile;
-  // q_full, k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], s_full[2], dp_full, dp_free,
-  // ds_ready[2], drain
-  static constexpr uint32_t kNumBars = 1 + 2 * KR + 2 * VR + 7;
+  // k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], q_ready, do_full, s_full, s_free,
+  // (unused), dp_free, ds_ready, (unused), drain; dP written and dQ done are the V and K
+  // slots' release barriers
+  static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 9;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
+  static constexpr uint32_t kColQ = 0, kColS = 64, kColDP = 192, kColDS = 320, kColDQ = 384;
   static_assert(kBytes <= 232448, "shared memory per block");
 };
 
+// A [128 x 128] in tensor memory as 16-bit pairs (64 columns) times B [128 rows x D] in shared
+// memory read MN-major: D[128 x D] (+)= A B.
+__device__ __forceinline__ void mma_tmem_kt(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                            uint32_t idesc, bool accumulate) {
+  const uint64_t b_desc = make_sdesc_sw128(b_smem, kSub, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kBT / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + ((kk * 16 * 128) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// A [128 x D] in tensor memory as 16-bit pairs (D / 2 columns) times B^T, B [128 rows x D]
+// K-major in shared memory (64-column sub-tiles kSub apart): D[128 x 128] = A B^T.
+template <int D>
+__device__ __forceinline__ void mma_tmem_rows_t(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                                uint32_t idesc) {
+  const uint64_t b_desc = make_sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (((kk >> 2) * kSub + (kk & 3) * 32) >> 4), idesc,
+           kk > 0 ? 1u : 0u);
+}
+
+// Rows of a contiguous 16-bit [rows, D] tensor into tensor memory, thread = lane row: D / 2
+// 32-bit columns, two elements a column with the lower-indexed one in the low half (the A
+// operand layout of tcgen05.mma kind::f16).  A row past the end is written as zeros.
+template <int D>
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src, bool valid) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t w[32];
+    if (valid) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + c * 64);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 x = s4[i];
+        w[4 * i] = x.x;
+        w[4 * i + 1] = x.y;
+        w[4 * i + 2] = x.z;
+        w[4 * i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = 0u;
+    }
+    tmem_st32(taddr + c * 32, w);
+  }
+}
+
 template <int D, bool BF16, int KR, int VR>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using L = QLayout<D, KR, VR>;
@@ -524,16 +562,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + L::kBar;
-  const uint32_t bar_q = bars;
-#define K_FULL(s) (bars + 8u * (1 + (s)))
-#define K_EMPTY(s) (bars + 8u * (1 + KR + (s)))
-#define V_FULL(s) (bars + 8u * (1 + 2 * KR + (s)))
-#define V_EMPTY(s) (bars + 8u * (1 + 2 * KR + VR + (s)))
-  const uint32_t bar_sfull = bars + 8u * (1 + 2 * KR + 2 * VR);  // [2] S_t in buffer t % 2
-  const uint32_t bar_dp = bar_sfull + 16;               // dP_t written (commit)
-  const uint32_t bar_dpfree = bar_sfull + 24;           // dP_t read (256 arrivals)
-  const uint32_t bar_ds = bar_sfull + 32;               // [2] dS_t stored in buffer t % 2
-  const uint32_t bar_drain = bar_sfull + 48;
+#define K_FULL(s) (bars + 8u * (s))
+#define K_EMPTY(s) (bars + 8u * (KR + (s)))
+#define V_FULL(s) (bars + 8u * (2 * KR + (s)))
+#define V_EMPTY(s) (bars + 8u * (2 * KR + VR + (s)))
+  const uint32_t bar_q = bars + 8u * (2 * KR + 2 * VR);  // Q rows in tensor memory (128)
+  const uint32_t bar_do = bar_q + 8;         // dO tile landed (TMA)
+  const uint32_t bar_sfull = bar_q + 16;     // S_t written (MMA commit)
+  const uint32_t bar_sfree = bar_q + 24;     // S_t read (256 arrivals)
+  const uint32_t bar_dpfree = bar_q + 40;    // dP_t read (256 arrivals)
+  const uint32_t bar_ds = bar_q + 48;        // dS_t stored (256 arrivals)
+  const uint32_t bar_drain = bar_q + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -547,7 +586,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   kv_tile_range(qt, kBT, kBT, p.N_q, p.N_kv, p.causal, n, first_masked);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
     for (int s = 0; s < KR; ++s) {
       mbar_init(K_FULL(s), 1);
       mbar_init(K_EMPTY(s), 1);
@@ -556,12 +594,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(V_FULL(s), 1);
       mbar_init(V_EMPTY(s), 1);
     }
-    for (int bb = 0; bb < 2; ++bb) {
-      mbar_init(bar_sfull + 8u * bb, 1);
-      mbar_init(bar_ds + 8u * bb, 2 * kEwThreads);
-    }
-    mbar_init(bar_dp, 1);
+    mbar_init(bar_q, kEwThreads);
+    mbar_init(bar_do, 1);
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 2 * kEwThreads);
     mbar_init(bar_dpfree, 2 * kEwThreads);
+    mbar_init(bar_ds, 2 * kEwThreads);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -577,19 +615,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kBwdProducerWarp) {
     if (lane == 0 && n > 0) {
-      prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+      mbar_arrive_expect_tx(bar_do, L::kTile);
 #pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub) {
-        tma_load_3d(base + L::kQ + sub * kSub, &tm_q, bar_q, sub * 64, qt * kBT, bh);
-        tma_load_3d(base + L::kDO + sub * kSub, &tm_do, bar_q, sub * 64, qt * kBT, bh);
-      }
-      // K_t goes to K slot t % KR (freed by dQ_{t-KR}), V_t to V slot t % VR (freed by
-      // dP_{t-VR}, which comes much earlier): the K ring is the deeper one, so that S_{t+2},
-      // issued right after dQ_t, finds K_{t+2} loaded.
+      for (int sub = 0; sub < D / 64; ++sub)
+        tma_load_3d(base + L::kDO + sub * kSub, &tm_do, bar_do, sub * 64, qt * kBT, bh);
       int issued_k = 0, issued_v = 0;
       for (int t = 0; t < n; ++t) {
         const int sk = t % KR, sv = t % VR;
@@ -608,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       t * kBT, kv_plane);
         issued_v = t + 1;
       }
-      wait_bounded(bar_q, 0, nullptr, p.status, kBwdDrainNs);
+      wait_bounded(bar_do, 0, nullptr, p.status, kBwdDrainNs);
       for (int t = (issued_k > KR ? issued_k - KR : 0); t < issued_k; ++t)
         wait_bounded(K_FULL(t % KR), (t / KR) & 1, nullptr, p.status, kBwdDrainNs);
       for (int t = (issued_v > VR ? issued_v - VR : 0); t < issued_v; ++t)
@@ -619,43 +651,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
       constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
-      // S_t = Q K_t^T into buffer t % 2 (next written by S_{t+2}, issued after dQ_t, which
-      // reads dS_t there); dP_t = dO V_t^T once dP_{t-1} has been read; dQ += dS_t K_t.
-      const uint64_t q_desc = make_sdesc_sw128(base + L::kQ, 16, 1024);
-      const uint64_t do_desc = make_sdesc_sw128(base + L::kDO, 16, 1024);
       auto issue_s = [&](int t) -> bool {
         const int s = t % KR;
         if (!wait_bounded(K_FULL(s), (t / KR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColS + (t & 1) * 128, q_desc,
-                                       make_sdesc_sw128(base + L::kK + s * L::kTile, 16, 1024),
-                                       idesc_rr);
-        mma_commit(bar_sfull + 8u * (t & 1));
+        mma_tmem_rows_t<D>(tmem + L::kColS, tmem + L::kColQ, base + L::kK + s * L::kTile, idesc_rr);
+        mma_commit(bar_sfull);
         return true;
       };
       auto issue_dp = [&](int t) -> bool {
         const int s = t % VR;
         if (!wait_bounded(V_FULL(s), (t / VR) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColDP, do_desc,
+        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColDP, make_sdesc_sw128(base + L::kDO, 16, 1024),
                                        make_sdesc_sw128(base + L::kV + s * L::kTile, 16, 1024),
                                        idesc_rr);
-        mma_commit(bar_dp);
+        // one commit for both readers: the elementwise warps (dP_t written) and the producer
+        // (V slot free) wait on the V slot's barrier
         mma_commit(V_EMPTY(s));
         return true;
       };
-      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) && issue_s(0) && issue_dp(0) &&
-                (n < 2 || issue_s(1));
+      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) &&
+                wait_bounded(bar_do, 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0) && issue_dp(0);
+      }
       for (int t = 0; ok && t < n; ++t) {
-        const int s = t % KR;
+        // S_{t+1} once S_t has been read, dP_{t+1} once dP_t has been read, then
+        // dQ += dS_t K_t once dS_t is stored
+        if (!wait_bounded(bar_sfree, t & 1, abort_flag, p.status)) break;
+        if (t + 1 < n && !issue_s(t + 1)) break;
         if (!wait_bounded(bar_dpfree, t & 1, abort_flag, p.status)) break;
         if (t + 1 < n && !issue_dp(t + 1)) break;
-        if (!wait_bounded(bar_ds + 8u * (t & 1), (t >> 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(bar_ds, t & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_split_rows(tmem + L::kColDQ, tmem + L::kColS + (t & 1) * 128,
-                       base + L::kK + s * L::kTile, idesc_q, t > 0);  // dQ += dS K
-        mma_commit(K_EMPTY(s));
-        if (t + 2 < n) ok = issue_s(t + 2);
+        mma_tmem_kt(tmem + L::kColDQ, tmem + L::kColDS, base + L::kK + (t % KR) * L::kTile, idesc_q,
+                    t > 0);  // dQ += dS K
+        // one commit for both readers: the elementwise warps (dS buffer free) and the producer
+        // (K slot free) wait on the K slot's barrier
+        mma_commit(K_EMPTY(t % KR));
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -677,46 +712,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int lim = p.causal ? row + (p.N_kv - p.N_q) : p.N_kv - 1;  // last visible key of this row
     if (lim > p.N_kv - 1) lim = p.N_kv - 1;
     bool ok = true;
+    if (n > 0 && wg == 0) {
+      // warpgroup 0 writes the Q rows
+      const size_t qrow = (static_cast<size_t>(bh) * p.N_q + (row < p.N_q ? row : 0)) * D;
+      row_to_tmem<D>(row_tmem + L::kColQ, p.q + qrow, row < p.N_q);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_q);
+    }
+    const uint32_t s_col = L::kColS + c0, dp_col = L::kColDP + c0, ds_col = L::kColDS + wg * 32;
     for (int t = 0; t < n; ++t) {
-      const uint32_t s_col = L::kColS + (t & 1) * 128 + c0;
       const bool masked = t >= first_masked;
       const int rel = lim - (t * kBT + c0);  // last visible key, relative to this half tile
-      if (!ew_wait(bar_sfull + 8u * (t & 1), (t >> 1) & 1, abort_flag, p.status)) {
+      if (!ew_wait(bar_sfull, t & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld32(row_tmem + s_col, sv[0]);
+      tmem_ld32(row_tmem + s_col + 32, sv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_sfree);  // S_{t+1} may overwrite
       // p = 2^(s scale log2(e) - L log2(e)), one packed FMA a pair; the mask only on the tiles
       // that need it (the same for every row of the tile)
       float pv[64];
-      {
-        uint32_t sv[2][32];
-        tmem_ld32(row_tmem + s_col, sv[0]);
-        tmem_ld32(row_tmem + s_col + 32, sv[1]);
-        tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = h * 32 + e;
-            float a0, a1;
-            fma2(a0, a1, __uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1]), sl2, sl2, nl2, nl2);
-            if (masked) {
-              a0 = (col <= rel) ? a0 : -INFINITY;
-              a1 = (col + 1 <= rel) ? a1 : -INFINITY;
-            }
-            pv[col] = ex2(a0);
-            pv[col + 1] = ex2(a1);
+        for (int e = 0; e < 32; e += 2) {
+          const int col = h * 32 + e;
+          float a0, a1;
+          fma2(a0, a1, __uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1]), sl2, sl2, nl2, nl2);
+          if (masked) {
+            a0 = (col <= rel) ? a0 : -INFINITY;
+            a1 = (col + 1 <= rel) ? a1 : -INFINITY;
           }
-      }
-      if (!ew_wait(bar_dp, t & 1, abort_flag, p.status)) {
+          pv[col] = ex2(a0);
+          pv[col + 1] = ex2(a1);
+        }
+      // dP_t written: the commit that also frees V slot t % VR (its (t / VR)-th phase); the
+      // next phase needs dP_{t+VR}, which waits for this warpgroup's read of dP_{t+VR-1}
+      if (!ew_wait(V_EMPTY(t % VR), (t / VR) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t dpv[2][32];
-      tmem_ld32(row_tmem + L::kColDP + c0, dpv[0]);
-      tmem_ld32(row_tmem + L::kColDP + c0 + 32, dpv[1]);
+      tmem_ld32(row_tmem + dp_col, dpv[0]);
+      tmem_ld32(row_tmem + dp_col + 32, dpv[1]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar_dpfree);  // dP_{t+1} may overwrite
@@ -732,10 +777,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fma2(g0, g1, pv[col], pv[col + 1], u0, u1, 0.0f, 0.0f);
           dd[col >> 1] = pack2<BF16>(g0, g1);
         }
-      tmem_st32(row_tmem + s_col, dd);  // dS over the S columns already read
+      // the dS buffer: free once dQ += dS_{t-1} K_{t-1} has finished (the commit that also
+      // frees K slot (t-1) % KR; its next phase needs dS_{t-1+KR}, not yet written)
+      if (t > 0 && !ew_wait(K_EMPTY((t - 1) % KR), ((t - 1) / KR) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(row_tmem + ds_col, dd);  // keys c0 .. c0+63 as 16-bit pairs
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ds + 8u * (t & 1));
+      mbar_arrive(bar_ds);
     }
     if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
     if (ok && wg == 0) {
@@ -772,20 +824,19 @@ size_t bwd_workspace_bytes(int B, int Hq, int N_q) {
 template <int D, bool BF16>
 static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   constexpr int QS = (D == 128) ? 4 : 6;  // 64-query stages of the dK/dV kernel
-  constexpr int KR = (D == 128) ? 3 : 4;  // K slots of the dQ kernel
-  constexpr int VR = (D == 128) ? 2 : 4;  // V slots of the dQ kernel
+  constexpr int KR = (D == 128) ? 3 : 6;  // K slots of the dQ kernel
+  constexpr int VR = (D == 128) ? 3 : 6;  // V slots of the dQ kernel (dO takes one tile too)
   using LK = KvLayout<D, QS>;
   using LQ = QLayout<D, KR, VR>;
   const uint64_t bhq = static_cast<uint64_t>(a.B) * a.Hq;
   const uint64_t bhk = static_cast<uint64_t>(a.B) * a.Hkv;
   const uint64_t rb = static_cast<uint64_t>(D) * 2;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tk, tv, tdo;
   CUtensorMap tq64, tdo64;  // 64-row boxes: the stages of the dK/dV kernel
   if (!make_tmap_3d(&tq64, a.q, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kStepQ, 1) ||
       !make_tmap_3d(&tdo64, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kStepQ, 1))
     return -5;
-  if (!make_tmap_3d(&tq, a.q, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
-      !make_tmap_3d(&tdo, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
+  if (!make_tmap_3d(&tdo, a.dout, BF16, D, a.N_q, bhq, rb, rb * a.N_q, 64, kBT, 1) ||
       !make_tmap_3d(&tk, a.k, BF16, D, a.N_kv, bhk, rb, rb * a.N_kv, 64, kBT, 1) ||
       !make_tmap_3d(&tv, a.v, BF16, D, a.N_kv, bhk, rb, rb * a.N_kv, 64, kBT, 1))
     return -5;
@@ -829,7 +880,7 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   if (kv_blocks > 0x7fffffffull || q_blocks > 0x7fffffffull) return -2;
   kkv<<<static_cast<unsigned>(kv_blocks), kBwdThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p);
   if (cudaGetLastError() != cudaSuccess) return -5;
-  kq<<<static_cast<unsigned>(q_blocks), kBwdThreads, LQ::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  kq<<<static_cast<unsigned>(q_blocks), kBwdThreads, LQ::kBytes, stream>>>(tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
