@@ -172,21 +172,11 @@ struct KvLayout {
   static_assert(kBytes <= 232448, "shared memory per block");
 };
 
-// K-major A (128 rows x D, 64-column sub-tiles a_sub bytes apart) x K-major B^T (N rows x D,
-// sub-tiles b_sub apart): D[128 x N] = A B^T.
-template <int D>
-__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t a_sub,
-                                              uint32_t b_smem, uint32_t b_sub, uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    mma_ss(d_tmem, make_sdesc_sw128(a_smem + (kk >> 2) * a_sub + (kk & 3) * 32, 16, 1024),
-           make_sdesc_sw128(b_smem + (kk >> 2) * b_sub + (kk & 3) * 32, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
-}
-
-// The same from the descriptors of the operands' first K step: a descriptor's start address
-// field counts 16-byte units, so a later K step's descriptor is the first one plus a constant
-// (the issuing thread builds two descriptors per product instead of two per MMA).
+// K-major A (128 rows x D, 64-column sub-tiles A_SUB bytes apart) x K-major B^T (N rows x D,
+// sub-tiles B_SUB apart): D[128 x N] = A B^T, from the descriptors of the operands' first K
+// step: a descriptor's start address field counts 16-byte units, so a later K step's
+// descriptor is the first one plus a constant (the issuing thread builds two descriptors per
+// product instead of two per MMA).
 template <int D, uint32_t A_SUB, uint32_t B_SUB>
 __device__ __forceinline__ void mma_rows_rows_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc) {
