@@ -670,6 +670,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     [[maybe_unused]] const bool tracer = (threadIdx.x & 127) == 0;  // timestamp hooks only
     const int off = p.N_kv - p.N_q;
     const float sl2 = p.sl2;
+    // read once: the masked tiles' bounds (those tiles come once or twice an item, and their
+    // parameter reads would otherwise be fetched cold)
+    const int n_kv = p.N_kv, causal = p.causal, window = p.window;
     float* mrow = reinterpret_cast<float*>(gbase + L::kMrow);    // [row]
     float* lpart = reinterpret_cast<float*>(gbase + L::kLpart);  // [item parity][row]
     const uint32_t s_col = wg ? kColS1 : kColS0;
@@ -748,20 +751,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(sr[c][e]);
-        if (j >= it.first_masked) {
-          int lim = p.causal ? row + off : p.N_kv - 1;  // last visible key of this row
-          if (lim > p.N_kv - 1) lim = p.N_kv - 1;
-          const int rel = lim - j * kBlockN;
+        if (j >= it.first_masked || j < it.lo_masked) {
+          // Visible columns [lo, hi] of this row in this tile: hi from the causal bound or the
+          // ragged end, lo from the sliding window.  One code path for every masked tile, as
+          // four 32-column bit masks and one test per column: masked tiles come once or twice
+          // an item, so their code is fetched cold, and a short path costs less.
+          int hi = kBlockN - 1, lo = 0;
+          if (j >= it.first_masked) {
+            int lim = causal ? row + off : n_kv - 1;  // last visible key of this row
+            if (lim > n_kv - 1) lim = n_kv - 1;
+            hi = min(lim - j * kBlockN, kBlockN - 1);
+          }
+          if (j < it.lo_masked) lo = max(row + off - window - j * kBlockN, 0);
+          uint32_t vis[kBlockN / 32];
+#pragma unroll
+          for (int g = 0; g < kBlockN / 32; ++g) {
+            const int a = max(lo - 32 * g, 0), bb = min(hi - 32 * g, 31);
+            vis[g] = (a > bb) ? 0u : ((0xffffffffu >> (31 - bb)) & (0xffffffffu << a));
+          }
+          // x + 0 where visible, x + (-inf) where not: integer arithmetic, no per-column
+          // condition (each of which could otherwise become a divergent branch)
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
-            if (c > rel) x[c] = -INFINITY;
-        }
-        if (j < it.lo_masked) {
-          // first visible key of this row under the sliding window
-          const int rel = row + off - p.window - j * kBlockN;
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            if (c < rel) x[c] = -INFINITY;
+            x[c] += __uint_as_float((((vis[c >> 5] >> (c & 31)) & 1u) - 1u) & 0xff800000u);
         }
         // Row maximum of the tile: three-input max, eight independent chains.
         float mx[8];

@@ -63,6 +63,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same, suspending the thread until the phase completes or about `hint_ns` pass (the
+// instruction's suspend-time hint): a waiting warp then takes no issue slots from the warps
+// that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test of the same condition (its latency can overlap independent work).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -85,7 +101,9 @@ static __device__ __forceinline__ bool wait_bounded_slow(uint32_t bar, uint32_t 
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // suspended up to 100 us per attempt: the limit and the abort flag are still checked
+    // thousands of times a second
+    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
     if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       if (abort) *abort = 1;
