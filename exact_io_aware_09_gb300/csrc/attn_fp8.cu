@@ -88,19 +88,23 @@ __device__ __forceinline__ float scale_of(float amax) {
 // One block per (plane, 128-row tile) of Q or of K (blocks [0, q_blocks) take Q): rotate
 // (optional), tile amax, quantise.  The tile passes through shared memory twice so that global
 // memory sees only coalesced 16-byte accesses: the 16-bit rows are loaded by consecutive threads,
-// then thread r takes row r whole (padded rows, conflict-free 16-byte reads) and runs every
-// butterfly stage in registers, in the plain order (h = 1, 2, ..., d/2); its E4M3 codes go back
-// through shared memory and out as coalesced rows.
+// then threads 2r and 2r + 1 take channels 0-63 and 64-127 of row r and run the butterfly stages
+// h = 1 .. 32 in registers, in the plain order; stage h = 64 pairs the two threads (the lower
+// keeps a + b, the upper computes a - b from the value it receives: the same fp32 operations).
+// Their E4M3 codes go back through shared memory and out as coalesced rows.
+constexpr int kRotThreads = 2 * kT;
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kT)
+__global__ void __launch_bounds__(kRotThreads)
     fp8_rotate_quantize_kernel(const uint16_t* xq, const uint16_t* xk, const int8_t* signs,
                                float inv_sqrt_d, uint8_t* cq, uint8_t* ck, float* sq, float* sk,
                                int Nq, int Nk, int nqt, int nkt, int q_blocks) {
-  static_assert(D == 128, "one row of 128 channels per thread");
-  constexpr int kPitch = D * 2 + 16;  // bytes per staged 16-bit row (16-byte reads conflict-free)
-  constexpr int kCodePitch = D + 16;  // bytes per staged code row
+  static_assert(D == 128, "two 64-channel halves per row");
+  constexpr int kH = D / 2;            // channels per thread
+  constexpr int kPitch = D * 2 + 16;   // bytes per staged 16-bit row
+  constexpr int kCodePitch = D + 16;   // bytes per staged code row
   __shared__ __align__(16) uint8_t stage[kT * kPitch];
-  __shared__ float red[kT / 32];
+  __shared__ float red[kRotThreads / 32];
   const bool is_q = static_cast<int>(blockIdx.x) < q_blocks;
   const int b = is_q ? blockIdx.x : blockIdx.x - q_blocks;
   const int n_tiles = is_q ? nqt : nkt;
@@ -109,30 +113,34 @@ __global__ void __launch_bounds__(kT)
   uint8_t* codes = is_q ? cq : ck;
   const int plane = b / n_tiles, tile = b % n_tiles;
   const int rows = min(kT, N - tile * kT);
+  const int my_row = threadIdx.x >> 1, half = threadIdx.x & 1;
   const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (static_cast<size_t>(plane) * N +
                                                                static_cast<size_t>(tile) * kT) * D);
   // 1. coalesced load of the tile's rows (rows past the end read as zeros)
   constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of a row
 #pragma unroll 4
-  for (int u = threadIdx.x; u < kT * kChunks; u += kT) {
+  for (int u = threadIdx.x; u < kT * kChunks; u += kRotThreads) {
     const int row = u / kChunks, c = u % kChunks;
     const uint4 w = row < rows ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D * 2 + c * 16)
                                : make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(stage + row * kPitch + c * 16) = w;
   }
-  // signs as four 32-bit masks (bit c set: channel c is negated), the same in every thread
-  uint32_t neg[D / 32] = {};
+  // signs of this thread's 64 channels as two 32-bit masks (bit c set: channel negated)
+  uint32_t neg[kH / 32] = {};
   if (signs) {
     const int lane = threadIdx.x & 31;
+    uint32_t all[D / 32];
 #pragma unroll
-    for (int q = 0; q < D / 32; ++q) neg[q] = __ballot_sync(0xffffffffu, signs[q * 32 + lane] < 0);
+    for (int q = 0; q < D / 32; ++q) all[q] = __ballot_sync(0xffffffffu, signs[q * 32 + lane] < 0);
+#pragma unroll
+    for (int q = 0; q < kH / 32; ++q) neg[q] = half ? all[kH / 32 + q] : all[q];
   }
   __syncthreads();
-  // 2. thread r: row r
-  float v[D];
+  // 2. this thread's half row
+  float v[kH];
 #pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(stage + threadIdx.x * kPitch + c * 16);
+  for (int c = 0; c < kH / 8; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + my_row * kPitch + half * kH * 2 + c * 16);
     float f[8];
     load8_words<BF16>(w, f);
 #pragma unroll
@@ -140,28 +148,34 @@ __global__ void __launch_bounds__(kT)
   }
   if (signs) {
 #pragma unroll
-    for (int c = 0; c < D; ++c)
+    for (int c = 0; c < kH; ++c)
       v[c] = __int_as_float(__float_as_int(v[c]) ^ (((neg[c >> 5] >> (c & 31)) & 1u) << 31));
 #pragma unroll
-    for (int h = 1; h < D; h <<= 1)
+    for (int h = 1; h < kH; h <<= 1)
 #pragma unroll
-      for (int j = 0; j < D; ++j)
+      for (int j = 0; j < kH; ++j)
         if ((j & h) == 0) {
           const float a = v[j], c = v[j + h];
           v[j] = a + c;
           v[j + h] = a - c;
         }
+    // h = 64: element j of the lower half with element j of the upper half
 #pragma unroll
-    for (int c = 0; c < D; ++c) v[c] = v[c] * inv_sqrt_d;
+    for (int j = 0; j < kH; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+      v[j] = half ? other - v[j] : v[j] + other;
+    }
+#pragma unroll
+    for (int c = 0; c < kH; ++c) v[c] = v[c] * inv_sqrt_d;
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int c = 0; c < D; ++c) amax = fmaxf(amax, fabsf(v[c]));
+  for (int c = 0; c < kH; ++c) amax = fmaxf(amax, fabsf(v[c]));
   // 3. tile amax, scale, codes (the block reduction's barriers also end every read of the stage)
   const float scale = scale_of(block_max(amax, red));
   if (threadIdx.x == 0) (is_q ? sq : sk)[b] = scale;
 #pragma unroll
-  for (int c = 0; c < D; c += 16) {
+  for (int c = 0; c < kH; c += 16) {
     uint4 w;
     w.x = pack4_e4m3(__fdiv_rn(v[c + 0], scale), __fdiv_rn(v[c + 1], scale),
                      __fdiv_rn(v[c + 2], scale), __fdiv_rn(v[c + 3], scale));
@@ -171,14 +185,14 @@ __global__ void __launch_bounds__(kT)
                      __fdiv_rn(v[c + 10], scale), __fdiv_rn(v[c + 11], scale));
     w.w = pack4_e4m3(__fdiv_rn(v[c + 12], scale), __fdiv_rn(v[c + 13], scale),
                      __fdiv_rn(v[c + 14], scale), __fdiv_rn(v[c + 15], scale));
-    *reinterpret_cast<uint4*>(stage + threadIdx.x * kCodePitch + c) = w;
+    *reinterpret_cast<uint4*>(stage + my_row * kCodePitch + half * kH + c) = w;
   }
   __syncthreads();
   // 4. coalesced store of the code rows
   uint8_t* dst = codes + (static_cast<size_t>(plane) * N + static_cast<size_t>(tile) * kT) * D;
   constexpr int kCodeChunks = D / 16;
 #pragma unroll 4
-  for (int u = threadIdx.x; u < kT * kCodeChunks; u += kT) {
+  for (int u = threadIdx.x; u < kT * kCodeChunks; u += kRotThreads) {
     const int row = u / kCodeChunks, c = u % kCodeChunks;
     if (row < rows)
       *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * D + c * 16) =
@@ -302,7 +316,7 @@ int launch_attn_fwd_fp8(const FwdArgs& a, const int8_t* signs, void* workspace,
   auto run = [&](auto bf16_tag) -> int {
     constexpr bool BF = decltype(bf16_tag)::value;
     const uint16_t* v16 = static_cast<const uint16_t*>(a.v);
-    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kT, 0, stream>>>(
+    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kRotThreads, 0, stream>>>(
         static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), signs, inv_sqrt_d,
         static_cast<uint8_t*>(const_cast<void*>(f.q8)), static_cast<uint8_t*>(const_cast<void*>(f.k8)),
         const_cast<float*>(f.q_scale), const_cast<float*>(f.k_scale), a.N_q, a.N_kv, nqt, nkt,
