@@ -17,18 +17,20 @@
 // S and dP are recomputed in both kernels (seven MMAs per tile pair instead of five): the price
 // of owning every output without atomics.
 //
-// Both kernels use 128 x 128 x 16 MMAs only (a tcgen05.mma takes about as long at N = 64 as at
-// N = 128, so narrower steps waste the tensor pipe), and two elementwise warpgroups that split
-// each tile's 128 columns.  The elementwise step writes its 16-bit results over the fp32
-// columns it has already read, which frees the dP buffer as soon as it has been read, so that
-// the next tile's dP product overlaps this tile's dS step.
+// The dK/dV kernel steps through 64 queries at a time (S^T and dP^T as 128 x 64 products,
+// double-buffered, so one step's elementwise work overlaps the next step's products); the dQ
+// kernel takes whole 128 x 128 tiles with single S and dP buffers that are released as soon as
+// they have been read.  The two elementwise warpgroups take alternate steps in kernel 1 and
+// split each tile's keys in kernel 2.  Probabilities and dS go back to tensor memory as 16-bit
+// pairs (over the fp32 columns they came from, or into a buffer of their own) and feed the
+// accumulating MMAs as their A operand.
 //
-// Roles inside a thread block (320 threads): warps 0-3 and 4-7 two elementwise warpgroups, one
-// per half of a tile's columns (thread = one row of the tensor-memory tiles: a key in kernel 1,
-// a query in kernel 2), warp 8 the TMA producer, warp 9 the tcgen05 issuer (and the
-// tensor-memory allocation).  Probabilities and dS go back to
-// tensor memory as 16-bit pairs, in place over the fp32 tiles they came from, and feed the next
-// MMAs as their A operand.  Every wait on a barrier is bounded.
+// Roles inside a thread block (352 threads): warps 0-3 and 4-7 the elementwise warpgroups
+// (thread = one row of the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 8
+// the TMA producer, warp 9 the issuer of the score-side products (S or S^T, dP or dP^T; it also
+// owns the tensor-memory allocation), warp 10 the issuer of the accumulations (dK and dV, or dQ).
+// Each issuing thread commits its own products; the hand-offs between them run through the
+// elementwise warps' barriers.  Every wait on a barrier is bounded.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,9 +39,12 @@ namespace attn {
 namespace {
 
 constexpr int kBT = 128;            // rows of a query tile and keys of a key tile
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr int kEwThreads = 128;     // one elementwise warpgroup (two of them: warps 0-3, 4-7)
-constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9;
+// warp 9 issues the score-side products (and owns the tensor-memory allocation), warp 10 the
+// gradient accumulations: two issuing threads keep the tensor pipe's short queue fed while one
+// of them waits on a barrier
+constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9, kBwdAccWarp = 10;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzled sub-tile
 constexpr uint64_t kBwdDrainNs = 100000000ull;
@@ -163,8 +168,9 @@ struct KvLayout {
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
-  // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], pds_ready[2], drain
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 7;
+  // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], pds_ready[2], drain,
+  // buf_free[2], drain of the score-side issuer
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 10;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -216,7 +222,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #define S_FULL(b) (bar_b + 8u * (b))           // S^T of buffer b written (MMA commit)
 #define DP_FULL(b) (bar_b + 8u * (2 + (b)))     // dP^T of buffer b written (MMA commit)
 #define PDS_READY(b) (bar_b + 8u * (4 + (b)))   // P^T and dS^T of buffer b stored (128 arrivals)
+#define BUF_FREE(b) (bar_b + 8u * (7 + (b)))    // dV and dK products of buffer b done (commit)
   const uint32_t bar_drain = bar_b + 8u * 6;
+  const uint32_t bar_drain_s = bar_b + 8u * 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -250,8 +258,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(S_FULL(bb), 1);
       mbar_init(DP_FULL(bb), 1);
       mbar_init(PDS_READY(bb), kEwThreads);
+      mbar_init(BUF_FREE(bb), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain_s, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -303,19 +313,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
+      // Step i in buffer i % 2: S^T_i = K Q_i^T and dP^T_i = V dO_i^T, once step i - 2's dV and
+      // dK products (which read P^T and dS^T from the same columns) are done.  The elementwise
+      // warpgroups and the other issuer run behind this thread, so it is normally two steps
+      // ahead of the accumulations.
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBT, kStepQ, false);
-      constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
-      // Step i in buffer i % 2: S^T_i = K Q_i^T and dP^T_i = V dO_i^T; once P^T_i and dS^T_i
-      // are stored, dV += P^T_i dO_i and dK += dS^T_i Q_i; then step i + 2's products into the
-      // same buffer (the MMAs of one thread run in issue order).  The elementwise warpgroups
-      // run ahead of the issuer, so the waits below are normally satisfied already: one wait
-      // per step, and descriptors built once per product, keep the issuing thread's work
-      // between MMAs small (the tensor pipe queues only one or two of them).
       const uint64_t dk_desc = make_sdesc_sw128(base + L::kK, 16, 1024);
       const uint64_t dv_desc = make_sdesc_sw128(base + L::kV, 16, 1024);
-      auto issue_sdp = [&](int i) -> bool {
+      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status);
+      for (int i = 0; ok && i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
-        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) return false;
+        if (i >= 2 && !wait_bounded(BUF_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t st = base + L::kStages + s * L::kStage;
         mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColS + bb * kStepQ, dk_desc,
@@ -324,11 +333,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColDP + bb * kStepQ, dv_desc,
                                                make_sdesc_sw128(st + L::kHalf, 16, 1024), idesc_s);
         mma_commit(DP_FULL(bb));
-        return true;
-      };
-      bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status) && issue_sdp(0) &&
-                (n_steps < 2 || issue_sdp(1));
-      for (int i = 0; ok && i < n_steps; ++i) {
+      }
+      // this thread's products are complete before the block ends (after an abort as well)
+      mma_commit(bar_drain_s);
+      wait_bounded(bar_drain_s, 0, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == kBwdAccWarp) {
+    if (lane == 0 && n > 0) {
+      // Once P^T_i and dS^T_i are stored: dV += P^T_i dO_i and dK += dS^T_i Q_i.  Their commit
+      // frees the stage (step i's score products are complete: the elementwise warps waited for
+      // them before storing) and the buffer.
+      constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
+      for (int i = 0; i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
         const uint32_t st = base + L::kStages + s * L::kStage;
         if (!wait_bounded(PDS_READY(bb), (i >> 1) & 1, abort_flag, p.status)) break;
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 make_sdesc_sw128(st, L::kHalfSub, 1024), idesc_acc,
                                 i > 0);  // dK += dS^T Q
         mma_commit(ST_EMPTY(s));
-        if (i + 2 < n_steps) ok = issue_sdp(i + 2);
+        mma_commit(BUF_FREE(bb));
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -458,6 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #undef S_FULL
 #undef DP_FULL
 #undef PDS_READY
+#undef BUF_FREE
   tc_fence_before();
   __syncthreads();
   if (warp == kBwdIssuerWarp) {
@@ -483,8 +501,8 @@ struct QLayout {
   static constexpr uint32_t kV = kK + KR * kTile;    // V ring, VR slots
   static constexpr uint32_t kBar = kV + VR * kTile;
   // k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], q_ready, do_full, s_full, s_free,
-  // (unused), dp_free, ds_ready, (unused), drain; dP written and dQ done are the V and K
-  // slots' release barriers
+  // drain of the score-side issuer, dp_free, ds_ready, (unused), drain; dP written and dQ done
+  // are the V and K slots' release barriers
   static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 9;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
@@ -560,6 +578,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_do = bar_q + 8;         // dO tile landed (TMA)
   const uint32_t bar_sfull = bar_q + 16;     // S_t written (MMA commit)
   const uint32_t bar_sfree = bar_q + 24;     // S_t read (256 arrivals)
+  const uint32_t bar_drain_s = bar_q + 32;   // score-side issuer's products done (commit)
   const uint32_t bar_dpfree = bar_q + 40;    // dP_t read (256 arrivals)
   const uint32_t bar_ds = bar_q + 48;        // dS_t stored (256 arrivals)
   const uint32_t bar_drain = bar_q + 64;
@@ -591,6 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_dpfree, 2 * kEwThreads);
     mbar_init(bar_ds, 2 * kEwThreads);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain_s, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -639,41 +659,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
+      // S_t once S_{t-1} has been read, dP_t once dP_{t-1} has been read
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
-      constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
-      auto issue_s = [&](int t) -> bool {
-        const int s = t % KR;
-        if (!wait_bounded(K_FULL(s), (t / KR) & 1, abort_flag, p.status)) return false;
+      const uint64_t do_desc = make_sdesc_sw128(base + L::kDO, 16, 1024);
+      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) &&
+                wait_bounded(bar_do, 0, abort_flag, p.status);
+      for (int t = 0; ok && t < n; ++t) {
+        const int sk = t % KR, sv = t % VR;
+        if (t > 0 && !wait_bounded(bar_sfree, (t - 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(K_FULL(sk), (t / KR) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_tmem_rows_t<D>(tmem + L::kColS, tmem + L::kColQ, base + L::kK + s * L::kTile, idesc_rr);
+        mma_tmem_rows_t<D>(tmem + L::kColS, tmem + L::kColQ, base + L::kK + sk * L::kTile, idesc_rr);
         mma_commit(bar_sfull);
-        return true;
-      };
-      auto issue_dp = [&](int t) -> bool {
-        const int s = t % VR;
-        if (!wait_bounded(V_FULL(s), (t / VR) & 1, abort_flag, p.status)) return false;
+        if (t > 0 && !wait_bounded(bar_dpfree, (t - 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(V_FULL(sv), (t / VR) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColDP, make_sdesc_sw128(base + L::kDO, 16, 1024),
-                                       make_sdesc_sw128(base + L::kV + s * L::kTile, 16, 1024),
+        mma_rows_rows_d<D, kSub, kSub>(tmem + L::kColDP, do_desc,
+                                       make_sdesc_sw128(base + L::kV + sv * L::kTile, 16, 1024),
                                        idesc_rr);
         // one commit for both readers: the elementwise warps (dP_t written) and the producer
         // (V slot free) wait on the V slot's barrier
-        mma_commit(V_EMPTY(s));
-        return true;
-      };
-      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) &&
-                wait_bounded(bar_do, 0, abort_flag, p.status);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_s(0) && issue_dp(0);
+        mma_commit(V_EMPTY(sv));
       }
-      for (int t = 0; ok && t < n; ++t) {
-        // S_{t+1} once S_t has been read, dP_{t+1} once dP_t has been read, then
-        // dQ += dS_t K_t once dS_t is stored
-        if (!wait_bounded(bar_sfree, t & 1, abort_flag, p.status)) break;
-        if (t + 1 < n && !issue_s(t + 1)) break;
-        if (!wait_bounded(bar_dpfree, t & 1, abort_flag, p.status)) break;
-        if (t + 1 < n && !issue_dp(t + 1)) break;
+      // this thread's products are complete before the block ends (after an abort as well)
+      mma_commit(bar_drain_s);
+      wait_bounded(bar_drain_s, 0, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == kBwdAccWarp) {
+    if (lane == 0 && n > 0) {
+      // dQ += dS_t K_t once dS_t is stored (S_t, read by the elementwise warps before they
+      // stored dS_t, is complete, so the K slot is free after this product)
+      constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
+      for (int t = 0; t < n; ++t) {
         if (!wait_bounded(bar_ds, t & 1, abort_flag, p.status)) break;
         tc_fence_after();
         mma_tmem_kt(tmem + L::kColDQ, tmem + L::kColDS, base + L::kK + (t % KR) * L::kTile, idesc_q,
