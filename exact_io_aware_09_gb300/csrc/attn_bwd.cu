@@ -169,8 +169,8 @@ struct KvLayout {
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
   // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], pds_ready[2], drain,
-  // buf_free[2], drain of the score-side issuer
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 10;
+  // p_free[2], ds_free[2], drain of the score-side issuer
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 12;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -222,9 +222,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #define S_FULL(b) (bar_b + 8u * (b))           // S^T of buffer b written (MMA commit)
 #define DP_FULL(b) (bar_b + 8u * (2 + (b)))     // dP^T of buffer b written (MMA commit)
 #define PDS_READY(b) (bar_b + 8u * (4 + (b)))   // P^T and dS^T of buffer b stored (128 arrivals)
-#define BUF_FREE(b) (bar_b + 8u * (7 + (b)))    // dV and dK products of buffer b done (commit)
+#define P_FREE(b) (bar_b + 8u * (7 + (b)))      // dV product of buffer b done: S^T columns free
+#define DS_FREE(b) (bar_b + 8u * (9 + (b)))     // dK product of buffer b done: dP^T columns free
   const uint32_t bar_drain = bar_b + 8u * 6;
-  const uint32_t bar_drain_s = bar_b + 8u * 9;
+  const uint32_t bar_drain_s = bar_b + 8u * 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -258,7 +259,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(S_FULL(bb), 1);
       mbar_init(DP_FULL(bb), 1);
       mbar_init(PDS_READY(bb), kEwThreads);
-      mbar_init(BUF_FREE(bb), 1);
+      mbar_init(P_FREE(bb), 1);
+      mbar_init(DS_FREE(bb), 1);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_s, 1);
@@ -313,23 +315,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
-      // Step i in buffer i % 2: S^T_i = K Q_i^T and dP^T_i = V dO_i^T, once step i - 2's dV and
-      // dK products (which read P^T and dS^T from the same columns) are done.  The elementwise
-      // warpgroups and the other issuer run behind this thread, so it is normally two steps
-      // ahead of the accumulations.
+      // Step i in buffer i % 2: S^T_i = K Q_i^T once step i - 2's dV product (which reads P^T
+      // from the same columns) is done, and dP^T_i = V dO_i^T once step i - 2's dK product
+      // (dS^T) is done.  Waiting for each product separately lets S^T_i start while dK_{i-2}
+      // is still running, so the tensor pipe does not drain between steps.
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBT, kStepQ, false);
       const uint64_t dk_desc = make_sdesc_sw128(base + L::kK, 16, 1024);
       const uint64_t dv_desc = make_sdesc_sw128(base + L::kV, 16, 1024);
       bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status);
       for (int i = 0; ok && i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
-        if (i >= 2 && !wait_bounded(BUF_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
         if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) break;
+        if (i >= 2 && !wait_bounded(P_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t st = base + L::kStages + s * L::kStage;
         mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColS + bb * kStepQ, dk_desc,
                                                make_sdesc_sw128(st, 16, 1024), idesc_s);
         mma_commit(S_FULL(bb));
+        if (i >= 2 && !wait_bounded(DS_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
         mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColDP + bb * kStepQ, dv_desc,
                                                make_sdesc_sw128(st + L::kHalf, 16, 1024), idesc_s);
         mma_commit(DP_FULL(bb));
@@ -341,9 +345,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdAccWarp) {
     if (lane == 0 && n > 0) {
-      // Once P^T_i and dS^T_i are stored: dV += P^T_i dO_i and dK += dS^T_i Q_i.  Their commit
-      // frees the stage (step i's score products are complete: the elementwise warps waited for
-      // them before storing) and the buffer.
+      // Once P^T_i and dS^T_i are stored: dV += P^T_i dO_i (its commit frees the S^T columns)
+      // and dK += dS^T_i Q_i (its commit frees the dP^T columns and the stage: step i's score
+      // products are complete, the elementwise warps waited for them before storing).
       constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
       for (int i = 0; i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
@@ -353,11 +357,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_tmem_rows_d<kStepQ>(tmem + L::kColDV, tmem + L::kColS + bb * kStepQ,
                                 make_sdesc_sw128(st + L::kHalf, L::kHalfSub, 1024), idesc_acc,
                                 i > 0);  // dV += P^T dO
+        mma_commit(P_FREE(bb));
         mma_tmem_rows_d<kStepQ>(tmem + L::kColDK, tmem + L::kColDP + bb * kStepQ,
                                 make_sdesc_sw128(st, L::kHalfSub, 1024), idesc_acc,
                                 i > 0);  // dK += dS^T Q
         mma_commit(ST_EMPTY(s));
-        mma_commit(BUF_FREE(bb));
+        mma_commit(DS_FREE(bb));
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -475,7 +480,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #undef S_FULL
 #undef DP_FULL
 #undef PDS_READY
-#undef BUF_FREE
+#undef P_FREE
+#undef DS_FREE
   tc_fence_before();
   __syncthreads();
   if (warp == kBwdIssuerWarp) {
