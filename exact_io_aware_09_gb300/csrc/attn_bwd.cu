@@ -168,9 +168,9 @@ struct KvLayout {
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
-  // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], pds_ready[2], drain,
-  // p_free[2], ds_free[2], drain of the score-side issuer
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 12;
+  // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], p_ready[2], drain,
+  // p_free[2], ds_free[2], drain of the score-side issuer, ds_ready[2]
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 14;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_b = bars + 8u * (1 + 2 * QS);
 #define S_FULL(b) (bar_b + 8u * (b))           // S^T of buffer b written (MMA commit)
 #define DP_FULL(b) (bar_b + 8u * (2 + (b)))     // dP^T of buffer b written (MMA commit)
-#define PDS_READY(b) (bar_b + 8u * (4 + (b)))   // P^T and dS^T of buffer b stored (128 arrivals)
+#define P_READY(b) (bar_b + 8u * (4 + (b)))     // P^T of buffer b stored (128 arrivals)
+#define DS_READY(b) (bar_b + 8u * (12 + (b)))   // dS^T of buffer b stored (128 arrivals)
 #define P_FREE(b) (bar_b + 8u * (7 + (b)))      // dV product of buffer b done: S^T columns free
 #define DS_FREE(b) (bar_b + 8u * (9 + (b)))     // dK product of buffer b done: dP^T columns free
   const uint32_t bar_drain = bar_b + 8u * 6;
@@ -258,7 +259,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int bb = 0; bb < 2; ++bb) {
       mbar_init(S_FULL(bb), 1);
       mbar_init(DP_FULL(bb), 1);
-      mbar_init(PDS_READY(bb), kEwThreads);
+      mbar_init(P_READY(bb), kEwThreads);
+      mbar_init(DS_READY(bb), kEwThreads);
       mbar_init(P_FREE(bb), 1);
       mbar_init(DS_FREE(bb), 1);
     }
@@ -345,19 +347,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdAccWarp) {
     if (lane == 0 && n > 0) {
-      // Once P^T_i and dS^T_i are stored: dV += P^T_i dO_i (its commit frees the S^T columns)
-      // and dK += dS^T_i Q_i (its commit frees the dP^T columns and the stage: step i's score
-      // products are complete, the elementwise warps waited for them before storing).
+      // Once P^T_i is stored: dV += P^T_i dO_i (its commit frees the S^T columns); once dS^T_i
+      // is stored: dK += dS^T_i Q_i (its commit frees the dP^T columns and the stage: step i's
+      // score products are complete, the elementwise warps waited for them before storing).
       constexpr uint32_t idesc_acc = make_idesc_f16(BF16, kBT, D, true);
       for (int i = 0; i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
         const uint32_t st = base + L::kStages + s * L::kStage;
-        if (!wait_bounded(PDS_READY(bb), (i >> 1) & 1, abort_flag, p.status)) break;
+        if (!wait_bounded(P_READY(bb), (i >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         mma_tmem_rows_d<kStepQ>(tmem + L::kColDV, tmem + L::kColS + bb * kStepQ,
                                 make_sdesc_sw128(st + L::kHalf, L::kHalfSub, 1024), idesc_acc,
                                 i > 0);  // dV += P^T dO
         mma_commit(P_FREE(bb));
+        if (!wait_bounded(DS_READY(bb), (i >> 1) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
         mma_tmem_rows_d<kStepQ>(tmem + L::kColDK, tmem + L::kColDP + bb * kStepQ,
                                 make_sdesc_sw128(st, L::kHalfSub, 1024), idesc_acc,
                                 i > 0);  // dK += dS^T Q
@@ -431,6 +435,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
       }
       tmem_st32(row_tmem + s_col, pp);  // P^T over the S^T columns already read
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(P_READY(wg));  // dV += P^T dO may start while dS^T is formed
       if (!ew_wait(DP_FULL(wg), (i >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
@@ -458,9 +465,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dd[(col >> 1) + 1] = pack2<BF16>(g2, g3);
         }
       tmem_st32(row_tmem + dp_col, dd);  // dS^T over the dP^T columns already read
-      tmem_wait_st();  // both stores (P^T and dS^T) have landed
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(PDS_READY(wg));
+      mbar_arrive(DS_READY(wg));
     }
     // epilogue: warpgroup 0 stores dV, warpgroup 1 dK, once the last MMA has finished
     if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
@@ -479,7 +486,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #undef ST_EMPTY
 #undef S_FULL
 #undef DP_FULL
-#undef PDS_READY
+#undef P_READY
+#undef DS_READY
 #undef P_FREE
 #undef DS_FREE
   tc_fence_before();
