@@ -515,24 +515,27 @@ struct QLayout {
   static constexpr uint32_t kV = kK + KR * kTile;    // V ring, VR slots
   static constexpr uint32_t kBar = kV + VR * kTile;
   // k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], q_ready, do_full, s_full, s_free,
-  // drain of the score-side issuer, dp_free, ds_ready, (unused), drain; dP written and dQ done
-  // are the V and K slots' release barriers
-  static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 9;
+  // drain of the score-side issuer, dp_free, ds_ready[2], drain, ds_free[2]; dP written is the
+  // V slot's release barrier
+  static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 11;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColQ = 0, kColS = 64, kColDP = 192, kColDS = 320, kColDQ = 384;
   static_assert(kBytes <= 232448, "shared memory per block");
 };
 
-// A [128 x 128] in tensor memory as 16-bit pairs (64 columns) times B [128 rows x D] in shared
-// memory read MN-major: D[128 x D] (+)= A B.
-__device__ __forceinline__ void mma_tmem_kt(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                            uint32_t idesc, bool accumulate) {
+// Half h of A [128 x 128] B: A in tensor memory as 16-bit pairs (64 columns), B [128 rows x D]
+// in shared memory read MN-major; the product over A's columns and B's rows 64h .. 64h + 63:
+// D[128 x D] (+)= A[:, 64h:64h+64] B[64h:64h+64, :].
+__device__ __forceinline__ void mma_tmem_kt_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                                 uint32_t idesc, int h, bool accumulate) {
   const uint64_t b_desc = make_sdesc_sw128(b_smem, kSub, 1024);
 #pragma unroll
-  for (int kk = 0; kk < kBT / 16; ++kk)
+  for (int k4 = 0; k4 < kBT / 32; ++k4) {
+    const int kk = h * (kBT / 32) + k4;
     mma_ts(d_tmem, a_tmem + kk * 8, b_desc + ((kk * 16 * 128) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+           (accumulate || k4 > 0) ? 1u : 0u);
+  }
 }
 
 // A [128 x D] in tensor memory as 16-bit pairs (D / 2 columns) times B^T, B [128 rows x D]
@@ -594,7 +597,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_sfree = bar_q + 24;     // S_t read (256 arrivals)
   const uint32_t bar_drain_s = bar_q + 32;   // score-side issuer's products done (commit)
   const uint32_t bar_dpfree = bar_q + 40;    // dP_t read (256 arrivals)
-  const uint32_t bar_ds = bar_q + 48;        // dS_t stored (256 arrivals)
+#define DS_READY(w) (bar_q + 48 + 8u * (w))       // warpgroup w's half of dS_t stored (128)
+#define DS_FREE(w) (bar_q + 72 + 8u * (w))        // dQ's product over that half done (commit)
   const uint32_t bar_drain = bar_q + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
@@ -622,7 +626,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_sfull, 1);
     mbar_init(bar_sfree, 2 * kEwThreads);
     mbar_init(bar_dpfree, 2 * kEwThreads);
-    mbar_init(bar_ds, 2 * kEwThreads);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(DS_READY(w), kEwThreads);
+      mbar_init(DS_FREE(w), 1);
+    }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_s, 1);
     *abort_flag = 0;
@@ -702,17 +709,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdAccWarp) {
     if (lane == 0 && n > 0) {
-      // dQ += dS_t K_t once dS_t is stored (S_t, read by the elementwise warps before they
-      // stored dS_t, is complete, so the K slot is free after this product)
+      // dQ += dS_t K_t in two halves over the keys, each once its warpgroup has stored its
+      // half of dS_t; each half's commit frees that half of the dS buffer.  After both, the K
+      // slot is free (S_t, read by the elementwise warps before they stored dS_t, is complete).
       constexpr uint32_t idesc_q = make_idesc_f16(BF16, kBT, D, true);
-      for (int t = 0; t < n; ++t) {
-        if (!wait_bounded(bar_ds, t & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        mma_tmem_kt(tmem + L::kColDQ, tmem + L::kColDS, base + L::kK + (t % KR) * L::kTile, idesc_q,
-                    t > 0);  // dQ += dS K
-        // one commit for both readers: the elementwise warps (dS buffer free) and the producer
-        // (K slot free) wait on the K slot's barrier
-        mma_commit(K_EMPTY(t % KR));
+      bool ok = true;
+      for (int t = 0; ok && t < n; ++t) {
+        const uint32_t kslot = base + L::kK + (t % KR) * L::kTile;
+        for (int w = 0; w < 2; ++w) {
+          if (!wait_bounded(DS_READY(w), t & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tmem_kt_half(tmem + L::kColDQ, tmem + L::kColDS, kslot, idesc_q, w,
+                           t > 0 || w > 0);  // dQ += dS K over keys 64w .. 64w + 63
+          mma_commit(DS_FREE(w));
+        }
+        if (ok) mma_commit(K_EMPTY(t % KR));
       }
       mma_commit(bar_drain);
       wait_bounded(bar_drain, 0, nullptr, p.status, kBwdDrainNs);
@@ -799,9 +813,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fma2(g0, g1, pv[col], pv[col + 1], u0, u1, 0.0f, 0.0f);
           dd[col >> 1] = pack2<BF16>(g0, g1);
         }
-      // the dS buffer: free once dQ += dS_{t-1} K_{t-1} has finished (the commit that also
-      // frees K slot (t-1) % KR; its next phase needs dS_{t-1+KR}, not yet written)
-      if (t > 0 && !ew_wait(K_EMPTY((t - 1) % KR), ((t - 1) / KR) & 1, abort_flag, p.status)) {
+      // this warpgroup's half of the dS buffer: free once dQ's product over it for tile t - 1
+      // has finished
+      if (t > 0 && !ew_wait(DS_FREE(wg), (t - 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -809,7 +823,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st32(row_tmem + ds_col, dd);  // keys c0 .. c0+63 as 16-bit pairs
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      mbar_arrive(DS_READY(wg));
     }
     if (ok && n > 0) ok = ew_wait(bar_drain, 0, abort_flag, p.status);
     if (ok && wg == 0) {
@@ -826,6 +840,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #undef K_EMPTY
 #undef V_FULL
 #undef V_EMPTY
+#undef DS_READY
+#undef DS_FREE
   tc_fence_before();
   __syncthreads();
   if (warp == kBwdIssuerWarp) {
