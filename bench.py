@@ -22,6 +22,7 @@ timed region.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -274,6 +275,12 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     pcfg = syn.CONFIG4
+    if args.prefill_heads != pcfg.Hq:
+        group = pcfg.Hq // pcfg.Hkv
+        if args.prefill_heads <= 0 or args.prefill_heads % group:
+            raise SystemExit(f"--prefill-heads must be a positive multiple of {group}")
+        pcfg = dataclasses.replace(pcfg, name=f"{pcfg.name}_hq{args.prefill_heads}",
+                                   Hq=args.prefill_heads, Hkv=args.prefill_heads // group)
     dcfg = syn.CONFIG5
     if args.decode_batch != dcfg.B:
         lens = tuple(int(x) for x in dcfg.lengths()[: args.decode_batch])
@@ -695,6 +702,9 @@ def main(argv=None):
                     help="run one half of the step (for profiling)")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="sequences of the decode workload (first B of the seeded lengths)")
+    ap.add_argument("--prefill-heads", type=int, default=64,
+                    help="query heads of the prefill workload (the key/value heads follow the "
+                         "group size; fewer heads make a smaller case for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
