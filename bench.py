@@ -648,7 +648,9 @@ def run_reference(args):
 
     pcfg = syn.CONFIG4
     q, k, v = pcfg.host_inputs()
-    rows_per_step = 16
+    # 1024 rows a step: the oracle's fixed cost per call (about 75 ms) stays a small part of
+    # the step, so the line reports the oracle's throughput rather than its call overhead
+    rows_per_step = 1024
     for i in range(args.warmup):
         oracle.attention_rows(q, k, v, pcfg.dtype, pcfg.B, pcfg.Hq, pcfg.Hkv, pcfg.N_q, pcfg.N_kv,
                               pcfg.d, True, pcfg.scale, prefill_sample_rows(pcfg, rows_per_step, 10_000 + i))
