@@ -605,9 +605,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // item: query tile qt of (batch, query head) bh; longest query tiles first
-  const int bh = blockIdx.x / p.n_qtiles;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
+  // item: query tile qt of (batch, query head) bh.  Query-tile major, last tile first: under
+  // the causal mask the longest items of every head start first and the grid ends on one-tile
+  // items; the heads of one key/value head run side by side and share its K/V tiles in L2.
+  const int n_bh = static_cast<int>(gridDim.x) / p.n_qtiles;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / n_bh;
+  const int bh = static_cast<int>(blockIdx.x) % n_bh;
   const int kv_plane = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.G;
   int n, first_masked;
   kv_tile_range(qt, kBT, kBT, p.N_q, p.N_kv, p.causal, n, first_masked);
