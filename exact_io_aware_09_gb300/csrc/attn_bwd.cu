@@ -550,29 +550,31 @@ __device__ __forceinline__ void mma_tmem_rows_t(uint32_t d_tmem, uint32_t a_tmem
            kk > 0 ? 1u : 0u);
 }
 
-// Rows of a contiguous 16-bit [rows, D] tensor into tensor memory, thread = lane row: D / 2
-// 32-bit columns, two elements a column with the lower-indexed one in the low half (the A
-// operand layout of tcgen05.mma kind::f16).  A row past the end is written as zeros.
+// One row of a contiguous 16-bit [rows, D] tensor as D / 2 32-bit words (zeros for a row past
+// the end), and those words into tensor memory, thread = lane row: two elements a column with
+// the lower-indexed one in the low half (the A operand layout of tcgen05.mma kind::f16).  The
+// load is issued before the block's setup, the store after it, so that the setup hides the
+// load's latency.
 template <int D>
-__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src, bool valid) {
+__device__ __forceinline__ void row_load(const uint16_t* src, bool valid, uint4 (&w)[D / 8]) {
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+    w[i] = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+}
+
+template <int D>
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint4 (&w)[D / 8]) {
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
-    uint32_t w[32];
-    if (valid) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src + c * 64);
+    uint32_t v[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 x = s4[i];
-        w[4 * i] = x.x;
-        w[4 * i + 1] = x.y;
-        w[4 * i + 2] = x.z;
-        w[4 * i + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = 0u;
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] = w[c * 8 + i].x;
+      v[4 * i + 1] = w[c * 8 + i].y;
+      v[4 * i + 2] = w[c * 8 + i].z;
+      v[4 * i + 3] = w[c * 8 + i].w;
     }
-    tmem_st32(taddr + c * 32, w);
+    tmem_st32(taddr + c * 32, v);
   }
 }
 
@@ -614,6 +616,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kv_plane = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.G;
   int n, first_masked;
   kv_tile_range(qt, kBT, kBT, p.N_q, p.N_kv, p.causal, n, first_masked);
+  // warpgroup 0 (thread = query row) starts loading the tile's Q rows now
+  uint4 q_row[D / 8];
+  if (n > 0 && threadIdx.x < kEwThreads) {
+    const int qr = qt * kBT + static_cast<int>(threadIdx.x);
+    row_load<D>(p.q + (static_cast<size_t>(bh) * p.N_q + (qr < p.N_q ? qr : 0)) * D, qr < p.N_q,
+                q_row);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KR; ++s) {
@@ -752,9 +761,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lim > p.N_kv - 1) lim = p.N_kv - 1;
     bool ok = true;
     if (n > 0 && wg == 0) {
-      // warpgroup 0 writes the Q rows
-      const size_t qrow = (static_cast<size_t>(bh) * p.N_q + (row < p.N_q ? row : 0)) * D;
-      row_to_tmem<D>(row_tmem + L::kColQ, p.q + qrow, row < p.N_q);
+      // warpgroup 0 writes the Q rows it loaded before the setup
+      row_to_tmem<D>(row_tmem + L::kColQ, q_row);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_q);
