@@ -2,8 +2,8 @@
 
 Small shapes cover several tiles, ragged query and key tails, bottom-right causal alignment,
 rows with no visible key, grouped-query heads, both head dimensions and both element types;
-the benchmark workloads run at full size (all rows, except the 8192-token GQA workload, whose
-rows are sampled).  Tolerances are those of tests/parity.py.
+the benchmark workloads run at full size, every row of every head.  Tolerances are those of
+tests/parity.py.
 """
 import numpy as np
 import pytest
@@ -164,17 +164,11 @@ def test_long_workload_full(attn, cfg):
     check_rows(og, lg, orf, lrf, cfg.name)
 
 
-def test_gqa_long_context_sampled(attn):
+def test_gqa_long_context_full(attn):
+    """The 70B-class GQA causal prefill (B=1, Hq=64, Hkv=8, N=8192, d=128, bf16): every row of
+    every head against the oracle."""
     cfg = syn.CONFIG4
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
-    rng = np.random.default_rng(4)
-    n = cfg.B * cfg.Hq * cfg.N_q
-    rows = np.unique(np.concatenate([
-        rng.integers(0, n, 6000),
-        # first and last rows of every head, and the rows around a tile boundary
-        np.arange(cfg.Hq) * cfg.N_q, np.arange(cfg.Hq) * cfg.N_q + cfg.N_q - 1,
-        np.arange(120, 140), cfg.N_q * 37 + np.arange(8000, 8192)])).astype(np.int64)
-    orf, lrf = oracle_rows(cfg, q, k, v, rows)
-    check_rows(og[rows], lg[rows], orf, lrf, cfg.name)
-    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
+    orf, lrf = oracle_rows(cfg, q, k, v)
+    check_rows(og, lg, orf, lrf, cfg.name)
