@@ -172,3 +172,17 @@ def fp8_attention(q, k, v, signs, causal, scale):
     qd, kd, vd = dequantized(prep, B, Hq, Hkv, Nq, Nkv, d)
     o, lse = attention_f64(qd, kd, vd, causal, scale)
     return o, lse, prep
+
+
+def fp8_attention_per_tensor(q, k, v, causal, scale):
+    """The baseline FP8 attention the pages compare incoherent processing against ("FlashAttention
+    Explained", section "FP8 Attention and Incoherent Processing"): no rotation and one scale per
+    tensor (amax of all of Q, of all of K, of all of V, over 448), then exact attention of the
+    dequantised operands.  q, k, v float32.  Returns (o, lse)."""
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    deq = []
+    for x in (q, k, v):
+        codes, sc = quantize_planes(np.asarray(x, np.float32).reshape(1, -1, d))
+        deq.append(e4m3_decode(codes).reshape(x.shape) * np.float64(sc[0]))
+    return attention_f64(deq[0], deq[1], deq[2], causal, scale)

@@ -142,3 +142,39 @@ def test_prepare_dequantises_to_the_rotated_inputs():
     # tile's other maxima; unrotated V keeps it whole
     assert prep["sq"][1 * Hq + 2, 1] > 1.5 * prep["sq"][1 * Hq + 2, 0]
     assert prep["sv"][0 * Hkv + 1] > 5 * prep["sv"][0 * Hkv + 0]
+
+
+def test_per_tensor_baseline_equals_block_scaling_when_every_block_shares_the_maximum():
+    """With the same amax in every 128-row tile of every Q and K plane and in every V plane, one
+    scale per tensor is the same as one per block: the baseline equals the unrotated block model
+    exactly."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, N, d = 1, 4, 2, 256, 64
+    q = rng.uniform(-1, 1, (B, Hq, N, d)).astype(np.float32)
+    k = rng.uniform(-1, 1, (B, Hkv, N, d)).astype(np.float32)
+    v = rng.uniform(-1, 1, (B, Hkv, N, d)).astype(np.float32)
+    for x in (q, k):
+        x[:, :, ::128, 0] = 2.0   # the first row of every tile holds the maximum
+    v[:, :, 0, 0] = 2.0
+    o_base, l_base = fp8.fp8_attention_per_tensor(q, k, v, True, d ** -0.5)
+    o_blk, l_blk, _ = fp8.fp8_attention(q, k, v, None, True, d ** -0.5)
+    np.testing.assert_array_equal(o_base, o_blk)
+    np.testing.assert_array_equal(l_base, l_blk)
+
+
+def test_per_tensor_baseline_lets_one_outlier_set_every_scale():
+    """One very large Q entry in head 0 sets the baseline's one scale for the whole tensor, which
+    pushes head 1's values (about 10^-5 of the outlier) into E4M3's subnormal range; the block
+    model gives head 1 a scale of its own.  Head 1's output error grows only in the baseline."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, N, d = 1, 2, 1, 128, 64
+    q = rng.standard_normal((B, Hq, N, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, N, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, N, d)).astype(np.float32)
+    q[0, 0, 3, 5] = 1.0e5
+    exact, _ = fp8.attention_f64(q.astype(np.float64), k.astype(np.float64),
+                                 v.astype(np.float64), False, d ** -0.5)
+    o_base, _ = fp8.fp8_attention_per_tensor(q, k, v, False, d ** -0.5)
+    o_blk, _, _ = fp8.fp8_attention(q, k, v, None, False, d ** -0.5)
+    err = lambda o: float(np.sqrt(np.mean((o[0, 1] - exact[0, 1]) ** 2)))
+    assert err(o_base) > 2 * err(o_blk), (err(o_base), err(o_blk))
