@@ -246,7 +246,7 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
  * allocates nothing.
  *
  *  - Limit: attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d) must not exceed
- *    attn_decode_static_scratch_bytes() (32 MiB, e.g. 16 sequences x 64 heads x 32k tokens at
+ *    attn_decode_static_scratch_bytes() (32 MiB, e.g. 15 sequences x 64 heads x 32k tokens at
  *    512-token splits, d = 128); larger requests return ATTN_ERR_WORKSPACE before any launch.
  *  - The first call on each device looks up that device's copy of the scratch array (with the
  *    device current); make that first call before any stream capture.
