@@ -518,10 +518,10 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
                          f"causal block pattern, {int(pattern.sum())} of {pattern.size} blocks"
                          if name == "block_sparse" else
                          "backward (dQ, dK, dV) of the causal GQA prefill, FLOPs by the pages' "
-                         "5-matmul count (2.5x forward); 3 launches" if name == "backward" else
+                         "5-matmul count (2.5x forward)" if name == "backward" else
                          "causal prefill in FP8 (E4M3) with a randomised Hadamard rotation of Q "
-                         "and K; each launch includes the rotation and quantisation (5 launches)")
-                        + " on the prefill workload's inputs",
+                         "and K; each launch includes the rotation and quantisation")
+                        + f" on the prefill workload's inputs; {args.steps} launches timed",
             "ms_per_launch": round(ms, 4), "flops_per_launch": flops, "value": round(tf, 1),
             "unit": "TFLOP/s",
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
