@@ -25,12 +25,13 @@
 // pairs (over the fp32 columns they came from, or into a buffer of their own) and feed the
 // accumulating MMAs as their A operand.
 //
-// Roles inside a thread block (352 threads): warps 0-3 and 4-7 the elementwise warpgroups
-// (thread = one row of the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 8
-// the TMA producer, warp 9 the issuer of the score-side products (S or S^T, dP or dP^T; it also
-// owns the tensor-memory allocation), warp 10 the issuer of the accumulations (dK and dV, or dQ).
-// Each issuing thread commits its own products; the hand-offs between them run through the
-// elementwise warps' barriers.  Every wait on a barrier is bounded.
+// Roles inside a thread block: warps 0-3 and 4-7 the elementwise warpgroups (thread = one row
+// of the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 8 the TMA producer,
+// warp 9 the issuer of the score products (S^T or S, and in kernel 2 also dP; it owns the
+// tensor-memory allocation), warp 10 the issuer of the accumulations (dV and dK, or dQ), and in
+// kernel 1 warp 11 the issuer of dP^T (384 threads; kernel 2 has 352).  Each issuing thread
+// commits its own products; the hand-offs between them run through the elementwise warps'
+// barriers.  Every wait on a barrier is bounded.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,12 +40,14 @@ namespace attn {
 namespace {
 
 constexpr int kBT = 128;            // rows of a query tile and keys of a key tile
-constexpr int kBwdThreads = 352;
+constexpr int kKvThreads = 384;    // dK/dV kernel: three issuing warps
+constexpr int kQThreads = 352;     // dQ kernel: two
 constexpr int kEwThreads = 128;     // one elementwise warpgroup (two of them: warps 0-3, 4-7)
 // warp 9 issues the score-side products (and owns the tensor-memory allocation), warp 10 the
-// gradient accumulations: two issuing threads keep the tensor pipe's short queue fed while one
-// of them waits on a barrier
-constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9, kBwdAccWarp = 10;
+// gradient accumulations; in the dK/dV kernel warp 11 takes the dP^T products off warp 9.
+// Several issuing threads keep the tensor pipe's short queue fed while one of them waits on a
+// barrier.
+constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9, kBwdAccWarp = 10, kBwdDpWarp = 11;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzled sub-tile
 constexpr uint64_t kBwdDrainNs = 100000000ull;
@@ -169,8 +172,8 @@ struct KvLayout {
   static constexpr uint32_t kStages = 2 * kTile;
   static constexpr uint32_t kBar = kStages + QS * kStage;
   // kv_full, st_full[QS], st_empty[QS], s_full[2], dp_full[2], p_ready[2], drain,
-  // p_free[2], ds_free[2], drain of the score-side issuer, ds_ready[2]
-  static constexpr uint32_t kNumBars = 1 + 2 * QS + 14;
+  // p_free[2], ds_free[2], drain of the S^T issuer, ds_ready[2], drain of the dP^T issuer
+  static constexpr uint32_t kNumBars = 1 + 2 * QS + 15;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -204,7 +207,7 @@ __device__ __forceinline__ void mma_tmem_rows_d(uint32_t d_tmem, uint32_t a_tmem
 }
 
 template <int D, bool BF16, int QS>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #define DS_FREE(b) (bar_b + 8u * (9 + (b)))     // dK product of buffer b done: dP^T columns free
   const uint32_t bar_drain = bar_b + 8u * 6;
   const uint32_t bar_drain_s = bar_b + 8u * 11;
+  const uint32_t bar_drain_dp = bar_b + 8u * 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -266,6 +270,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_s, 1);
+    mbar_init(bar_drain_dp, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -315,34 +320,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         wait_bounded(ST_FULL(i % QS), (i / QS) & 1, nullptr, p.status, kBwdDrainNs);
     }
     __syncwarp();
-  } else if (warp == kBwdIssuerWarp) {
+  } else if (warp == kBwdIssuerWarp || warp == kBwdDpWarp) {
     if (lane == 0 && n > 0) {
-      // Step i in buffer i % 2: S^T_i = K Q_i^T once step i - 2's dV product (which reads P^T
-      // from the same columns) is done, and dP^T_i = V dO_i^T once step i - 2's dK product
-      // (dS^T) is done.  Waiting for each product separately lets S^T_i start while dK_{i-2}
-      // is still running, so the tensor pipe does not drain between steps.
+      // Step i in buffer i % 2.  Warp 9: S^T_i = K Q_i^T once step i - 2's dV product (which
+      // reads P^T from the same columns) is done.  Warp 11: dP^T_i = V dO_i^T once step i - 2's
+      // dK product (dS^T) is done.  Waiting for each product separately lets step i's products
+      // start while step i - 2's are still in the pipe, and the two threads' waits overlap
+      // each other's issue.
+      const bool is_s = (warp == kBwdIssuerWarp);
       constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBT, kStepQ, false);
-      const uint64_t dk_desc = make_sdesc_sw128(base + L::kK, 16, 1024);
-      const uint64_t dv_desc = make_sdesc_sw128(base + L::kV, 16, 1024);
+      const uint64_t a_desc = make_sdesc_sw128(base + (is_s ? L::kK : L::kV), 16, 1024);
+      const uint32_t col0 = is_s ? L::kColS : L::kColDP;
+      const uint32_t b_off = is_s ? 0u : L::kHalf;  // Q or dO of the stage
       bool ok = wait_bounded(bar_kv, 0, abort_flag, p.status);
       for (int i = 0; ok && i < n_steps; ++i) {
         const int s = i % QS, bb = i & 1;
         if (!wait_bounded(ST_FULL(s), (i / QS) & 1, abort_flag, p.status)) break;
-        if (i >= 2 && !wait_bounded(P_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
+        if (i >= 2 && !wait_bounded(is_s ? P_FREE(bb) : DS_FREE(bb), ((i >> 1) - 1) & 1,
+                                    abort_flag, p.status))
+          break;
         tc_fence_after();
         const uint32_t st = base + L::kStages + s * L::kStage;
-        mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColS + bb * kStepQ, dk_desc,
-                                               make_sdesc_sw128(st, 16, 1024), idesc_s);
-        mma_commit(S_FULL(bb));
-        if (i >= 2 && !wait_bounded(DS_FREE(bb), ((i >> 1) - 1) & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + L::kColDP + bb * kStepQ, dv_desc,
-                                               make_sdesc_sw128(st + L::kHalf, 16, 1024), idesc_s);
-        mma_commit(DP_FULL(bb));
+        mma_rows_rows_d<D, kSub, L::kHalfSub>(tmem + col0 + bb * kStepQ, a_desc,
+                                               make_sdesc_sw128(st + b_off, 16, 1024), idesc_s);
+        mma_commit(is_s ? S_FULL(bb) : DP_FULL(bb));
       }
       // this thread's products are complete before the block ends (after an abort as well)
-      mma_commit(bar_drain_s);
-      wait_bounded(bar_drain_s, 0, nullptr, p.status, kBwdDrainNs);
+      const uint32_t drain = is_s ? bar_drain_s : bar_drain_dp;
+      mma_commit(drain);
+      wait_bounded(drain, 0, nullptr, p.status, kBwdDrainNs);
     }
     __syncwarp();
   } else if (warp == kBwdAccWarp) {
@@ -579,7 +585,7 @@ __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint4 (&w)[D /
 }
 
 template <int D, bool BF16, int KR, int VR>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -927,9 +933,9 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t kv_blocks = bhk * p.n_kvtiles;
   const uint64_t q_blocks = bhq * n_qtiles;
   if (kv_blocks > 0x7fffffffull || q_blocks > 0x7fffffffull) return -2;
-  kkv<<<static_cast<unsigned>(kv_blocks), kBwdThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p);
+  kkv<<<static_cast<unsigned>(kv_blocks), kKvThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p);
   if (cudaGetLastError() != cudaSuccess) return -5;
-  kq<<<static_cast<unsigned>(q_blocks), kBwdThreads, LQ::kBytes, stream>>>(tk, tv, tdo, p);
+  kq<<<static_cast<unsigned>(q_blocks), kQThreads, LQ::kBytes, stream>>>(tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
