@@ -25,13 +25,13 @@
 // pairs (over the fp32 columns they came from, or into a buffer of their own) and feed the
 // accumulating MMAs as their A operand.
 //
-// Roles inside a thread block: warps 0-3 and 4-7 the elementwise warpgroups (thread = one row
-// of the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 8 the TMA producer,
-// warp 9 the issuer of the score products (S^T or S, and in kernel 2 also dP; it owns the
-// tensor-memory allocation), warp 10 the issuer of the accumulations (dV and dK, or dQ), and in
-// kernel 1 warp 11 the issuer of dP^T (384 threads; kernel 2 has 352).  Each issuing thread
-// commits its own products; the hand-offs between them run through the elementwise warps'
-// barriers.  Every wait on a barrier is bounded.
+// Roles inside a thread block (384 threads): warps 0-3 and 4-7 the elementwise warpgroups
+// (thread = one row of the tensor-memory tiles: a key in kernel 1, a query in kernel 2), warp 8
+// the TMA producer, warp 9 the issuer of the score products (S^T or S; it owns the
+// tensor-memory allocation), warp 11 the issuer of dP^T or dP, warp 10 the issuer of the
+// accumulations (dV and dK, or dQ).  Each issuing thread commits its own products; the
+// hand-offs between them run through the elementwise warps' barriers.  Every wait on a barrier
+// is bounded.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,13 +40,12 @@ namespace attn {
 namespace {
 
 constexpr int kBT = 128;            // rows of a query tile and keys of a key tile
-constexpr int kKvThreads = 384;    // dK/dV kernel: three issuing warps
-constexpr int kQThreads = 352;     // dQ kernel: two
+constexpr int kKvThreads = 384;    // three issuing warps in either kernel
+constexpr int kQThreads = 384;
 constexpr int kEwThreads = 128;     // one elementwise warpgroup (two of them: warps 0-3, 4-7)
-// warp 9 issues the score-side products (and owns the tensor-memory allocation), warp 10 the
-// gradient accumulations; in the dK/dV kernel warp 11 takes the dP^T products off warp 9.
-// Several issuing threads keep the tensor pipe's short queue fed while one of them waits on a
-// barrier.
+// warp 9 issues the score products S^T or S (and owns the tensor-memory allocation), warp 11
+// the dP^T or dP products, warp 10 the gradient accumulations.  Several issuing threads keep
+// the tensor pipe's short queue fed while one of them waits on a barrier.
 constexpr int kBwdProducerWarp = 8, kBwdIssuerWarp = 9, kBwdAccWarp = 10, kBwdDpWarp = 11;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint32_t kSub = 128 * 128;  // bytes of one 64-column, 128-row swizzled sub-tile
@@ -521,9 +520,9 @@ struct QLayout {
   static constexpr uint32_t kV = kK + KR * kTile;    // V ring, VR slots
   static constexpr uint32_t kBar = kV + VR * kTile;
   // k_full[KR], k_empty[KR], v_full[VR], v_empty[VR], q_ready, do_full, s_full, s_free,
-  // drain of the score-side issuer, dp_free, ds_ready[2], drain, ds_free[2]; dP written is the
-  // V slot's release barrier
-  static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 11;
+  // drain of the S issuer, dp_free, ds_ready[2], drain, ds_free[2], drain of the dP issuer;
+  // dP written is the V slot's release barrier
+  static constexpr uint32_t kNumBars = 2 * KR + 2 * VR + 12;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16 + 1024;
   static constexpr uint32_t kColQ = 0, kColS = 64, kColDP = 192, kColDS = 320, kColDQ = 384;
@@ -603,7 +602,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t bar_do = bar_q + 8;         // dO tile landed (TMA)
   const uint32_t bar_sfull = bar_q + 16;     // S_t written (MMA commit)
   const uint32_t bar_sfree = bar_q + 24;     // S_t read (256 arrivals)
-  const uint32_t bar_drain_s = bar_q + 32;   // score-side issuer's products done (commit)
+  const uint32_t bar_drain_s = bar_q + 32;   // S issuer's products done (commit)
+  const uint32_t bar_drain_dp = bar_q + 88;  // dP issuer's products done (commit)
   const uint32_t bar_dpfree = bar_q + 40;    // dP_t read (256 arrivals)
 #define DS_READY(w) (bar_q + 48 + 8u * (w))       // warpgroup w's half of dS_t stored (128)
 #define DS_FREE(w) (bar_q + 72 + 8u * (w))        // dQ's product over that half done (commit)
@@ -650,6 +650,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_s, 1);
+    mbar_init(bar_drain_dp, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -698,18 +699,30 @@ __global__ void __launch_bounds__(kQThreads, 1)
     __syncwarp();
   } else if (warp == kBwdIssuerWarp) {
     if (lane == 0 && n > 0) {
-      // S_t once S_{t-1} has been read, dP_t once dP_{t-1} has been read
+      // S_t = Q K_t^T once S_{t-1} has been read
       constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
-      const uint64_t do_desc = make_sdesc_sw128(base + L::kDO, 16, 1024);
-      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status) &&
-                wait_bounded(bar_do, 0, abort_flag, p.status);
+      bool ok = wait_bounded(bar_q, 0, abort_flag, p.status);
       for (int t = 0; ok && t < n; ++t) {
-        const int sk = t % KR, sv = t % VR;
+        const int sk = t % KR;
         if (t > 0 && !wait_bounded(bar_sfree, (t - 1) & 1, abort_flag, p.status)) break;
         if (!wait_bounded(K_FULL(sk), (t / KR) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         mma_tmem_rows_t<D>(tmem + L::kColS, tmem + L::kColQ, base + L::kK + sk * L::kTile, idesc_rr);
         mma_commit(bar_sfull);
+      }
+      // this thread's products are complete before the block ends (after an abort as well)
+      mma_commit(bar_drain_s);
+      wait_bounded(bar_drain_s, 0, nullptr, p.status, kBwdDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == kBwdDpWarp) {
+    if (lane == 0 && n > 0) {
+      // dP_t = dO V_t^T once dP_{t-1} has been read
+      constexpr uint32_t idesc_rr = make_idesc_f16(BF16, kBT, kBT, false);
+      const uint64_t do_desc = make_sdesc_sw128(base + L::kDO, 16, 1024);
+      bool ok = wait_bounded(bar_do, 0, abort_flag, p.status);
+      for (int t = 0; ok && t < n; ++t) {
+        const int sv = t % VR;
         if (t > 0 && !wait_bounded(bar_dpfree, (t - 1) & 1, abort_flag, p.status)) break;
         if (!wait_bounded(V_FULL(sv), (t / VR) & 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -720,9 +733,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // (V slot free) wait on the V slot's barrier
         mma_commit(V_EMPTY(sv));
       }
-      // this thread's products are complete before the block ends (after an abort as well)
-      mma_commit(bar_drain_s);
-      wait_bounded(bar_drain_s, 0, nullptr, p.status, kBwdDrainNs);
+      mma_commit(bar_drain_dp);
+      wait_bounded(bar_drain_dp, 0, nullptr, p.status, kBwdDrainNs);
     }
     __syncwarp();
   } else if (warp == kBwdAccWarp) {
