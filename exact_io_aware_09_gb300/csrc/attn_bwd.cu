@@ -32,6 +32,14 @@
 // accumulations (dV and dK, or dQ).  Each issuing thread commits its own products; the
 // hand-offs between them run through the elementwise warps' barriers.  Every wait on a barrier
 // is bounded.
+#include <algorithm>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -160,6 +168,20 @@ __global__ void attn_bwd_pre_kernel(const uint16_t* o, const uint16_t* dout, con
 // 16-bit pairs over the first 32 columns of the buffers they came from.
 constexpr int kStepQ = 64;  // queries per step of the dK/dV kernel
 
+// Dispatch order of the dK/dV kernel's blocks.  A block's work grows with the query tiles that
+// see its key tile, and under the causal mask the longest blocks are long against a GPU's share
+// of the whole (a 128-key tile of an 8192-token sequence with eight query heads: 1,024 64-query
+// steps, against about 1,750 per SM): started longest first, the blocks leave a tail of about 7%.
+// The launcher packs the blocks into one bin per SM (largest first, each into the fullest bin
+// that stays under the average load) and lists them in the order in which SMs that free up in
+// turn would take them; block i of the launch then runs job order.job[i].  n = 0: the default
+// order (key tile major, job = block index).
+constexpr int kMaxKvOrder = 2048;
+struct KvOrder {
+  int n;
+  uint16_t job[kMaxKvOrder];
+};
+
 template <int D, int QS>
 struct KvLayout {
   static constexpr uint32_t kTile = kBT * D * 2;             // K or V: 128 rows
@@ -210,7 +232,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p,
+                         const __grid_constant__ KvOrder order) {
   using L = KvLayout<D, QS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -235,12 +258,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // item: key tile kt of (batch, key/value head) bkv
-  // key tile major: under the causal mask the first key tiles have the most query tiles, so
-  // every (batch, key/value head)'s longest items start first
+  // job: key tile kt of (batch, key/value head) bkv, numbered key tile major; the launch order
+  // is the packed one of KvOrder when the launcher gives one
   const int n_planes = static_cast<int>(gridDim.x / p.n_kvtiles);
-  const int kt = static_cast<int>(blockIdx.x / n_planes);
-  const int bkv = static_cast<int>(blockIdx.x % n_planes);
+  const int job = order.n ? static_cast<int>(order.job[blockIdx.x]) : static_cast<int>(blockIdx.x);
+  const int kt = job / n_planes;
+  const int bkv = job % n_planes;
   const int b = bkv / p.Hkv;
   const int hk = bkv % p.Hkv;
   const int off = p.N_kv - p.N_q;
@@ -888,6 +911,81 @@ size_t bwd_workspace_bytes(int B, int Hq, int N_q) {
   return static_cast<size_t>(B) * Hq * nqp * 8;  // L log2(e) and D, fp32
 }
 
+// 64-query steps of the dK/dV job for key tile kt (as the kernel counts them).
+static int kv_job_steps(int kt, int n_qtiles, int G, int causal, int off) {
+  int qt_lo = 0;
+  if (causal) {
+    const int first_row = kt * kBT - off;
+    qt_lo = first_row > 0 ? first_row / kBT : 0;
+  }
+  const int nq_per = n_qtiles - qt_lo;
+  return nq_per > 0 ? 2 * G * nq_per : 0;
+}
+
+// The packed dispatch order (KvOrder) for one shape, computed once and kept.
+static const KvOrder* kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal,
+                               int off) {
+  static const KvOrder kDefault = {0, {}};
+  const int n_jobs = n_planes * n_kvtiles;
+  int dev = 0, n_sm = 0;
+  if (!causal || n_jobs > kMaxKvOrder || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n_sm <= 0 || n_jobs <= n_sm)
+    return &kDefault;
+  using Key = std::tuple<int, int, int, int, int, int>;
+  static std::map<Key, std::unique_ptr<KvOrder>> cache;
+  static std::mutex mu;
+  const Key key{n_planes, n_kvtiles, n_qtiles, G, off, n_sm};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second.get();
+  // job weights: its steps plus a block's fixed cost (about four steps: setup, K/V load,
+  // pipeline fill, dK/dV store)
+  std::vector<long long> w(n_jobs);
+  long long total = 0;
+  for (int j = 0; j < n_jobs; ++j) {
+    w[j] = kv_job_steps(j / n_planes, n_qtiles, G, causal, off) + 4;
+    total += w[j];
+  }
+  std::vector<int> by_size(n_jobs);
+  for (int j = 0; j < n_jobs; ++j) by_size[j] = j;
+  std::stable_sort(by_size.begin(), by_size.end(), [&](int x, int y) { return w[x] > w[y]; });
+  const long long cap = (total + n_sm - 1) / n_sm;
+  std::vector<std::vector<int>> bins(n_sm);
+  std::vector<long long> load(n_sm, 0);
+  for (int j : by_size) {
+    int best = -1, emptiest = 0;
+    for (int b = 0; b < n_sm; ++b) {
+      if (load[b] + w[j] <= cap && (best < 0 || load[b] > load[best])) best = b;
+      if (load[b] < load[emptiest]) emptiest = b;
+    }
+    const int b = best >= 0 ? best : emptiest;
+    bins[b].push_back(j);  // largest first within a bin
+    load[b] += w[j];
+  }
+  // the order in which SMs that free up in turn take the bins' jobs
+  auto order = std::make_unique<KvOrder>();
+  order->n = 0;
+  using Slot = std::pair<long long, int>;  // (time the SM frees up, bin)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  std::vector<size_t> next(n_sm, 0);
+  for (int b = 0; b < n_sm; ++b) free_at.push({0, b});
+  while (!free_at.empty()) {
+    const Slot sl = free_at.top();
+    free_at.pop();
+    const int b = sl.second;
+    if (next[b] < bins[b].size()) {
+      const int j = bins[b][next[b]++];
+      order->job[order->n++] = static_cast<uint16_t>(j);
+      free_at.push({sl.first + w[j], b});
+    }
+  }
+  if (order->n != n_jobs) return &kDefault;
+  const KvOrder* out = order.get();
+  cache.emplace(key, std::move(order));
+  return out;
+}
+
 template <int D, bool BF16>
 static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   constexpr int QS = (D == 128) ? 4 : 6;  // 64-query stages of the dK/dV kernel
@@ -945,7 +1043,10 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t kv_blocks = bhk * p.n_kvtiles;
   const uint64_t q_blocks = bhq * n_qtiles;
   if (kv_blocks > 0x7fffffffull || q_blocks > 0x7fffffffull) return -2;
-  kkv<<<static_cast<unsigned>(kv_blocks), kKvThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p);
+  const KvOrder* order = kv_order(static_cast<int>(bhk), p.n_kvtiles, n_qtiles, p.G, a.causal,
+                                  a.N_kv - a.N_q);
+  kkv<<<static_cast<unsigned>(kv_blocks), kKvThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p,
+                                                                            *order);
   if (cudaGetLastError() != cudaSuccess) return -5;
   kq<<<static_cast<unsigned>(q_blocks), kQThreads, LQ::kBytes, stream>>>(tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -5;

@@ -76,6 +76,10 @@ SHAPES = [
     (1, 1, 1, 255, 1000, 128, "bf16", False),
     (2, 4, 4, 640, 640, 128, "bf16", False),
     (1, 16, 2, 1024, 1024, 128, "bf16", True),
+    # more dK/dV blocks than SMs under the causal mask: the blocks run in the launcher's packed
+    # order, and every key tile of every head must still be computed once
+    (2, 16, 8, 1280, 1280, 64, "bf16", True),
+    (1, 32, 16, 1280, 1280, 128, "f16", True),
 ]
 
 
