@@ -14,7 +14,8 @@ import os
 __all__ = [
     "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes",
     "attn_decode_splitkv_static", "attn_decode_static_scratch_bytes",
-    "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_selftest_timeout",
+    "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_bwd_kv_order",
+    "attn_selftest_timeout",
     "attn_version", "library_path", "lib",
 ]
 
@@ -69,6 +70,8 @@ lib.attn_status_string.argtypes = [_I]
 lib.attn_status_string.restype = ctypes.c_char_p
 lib.attn_fwd_kv_tiles.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
 lib.attn_fwd_kv_tiles.restype = _I
+lib.attn_bwd_kv_order.argtypes = [_I] * 7 + [ctypes.POINTER(ctypes.c_uint16), _I, ctypes.POINTER(_I)]
+lib.attn_bwd_kv_order.restype = _I
 lib.attn_fwd_kv_span.argtypes = [_I, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_I)] * 4
 lib.attn_fwd_kv_span.restype = _I
 lib.attn_selftest_timeout.argtypes = [_I, _P]
@@ -401,6 +404,17 @@ def attn_fwd_kv_tiles(q_tile: int, block_m: int, block_n: int, N_q: int, N_kv: i
     _check(lib.attn_fwd_kv_tiles(q_tile, block_m, block_n, N_q, N_kv, int(bool(causal)),
                                  ctypes.byref(n), ctypes.byref(fm)), "attn_fwd_kv_tiles")
     return n.value, fm.value
+
+
+def attn_bwd_kv_order(B: int, Hq: int, Hkv: int, N_q: int, N_kv: int, causal: bool, n_sm: int,
+                      cap: int = 2048):
+    """Launch order of attn_bwd's dK/dV blocks on n_sm SMs (host only): the job of every block,
+    or an empty list when the default order (job = block index) stands."""
+    buf = (ctypes.c_uint16 * max(cap, 1))()
+    n = _I(0)
+    _check(lib.attn_bwd_kv_order(B, Hq, Hkv, N_q, N_kv, int(bool(causal)), n_sm, buf, cap,
+                                 ctypes.byref(n)), "attn_bwd_kv_order")
+    return list(buf[:n.value])
 
 
 def attn_selftest_timeout(limit_us: int, stream=None) -> None:

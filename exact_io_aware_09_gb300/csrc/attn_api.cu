@@ -412,6 +412,17 @@ int attn_fwd_kv_tiles(int q_tile, int block_m, int block_n, int N_q, int N_kv, i
   return ATTN_OK;
 }
 
+int attn_bwd_kv_order(int B, int Hq, int Hkv, int N_q, int N_kv, int causal, int n_sm,
+                      uint16_t* job, int cap, int* n) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N_q < 0 || N_kv < 0 || n_sm <= 0 || !n ||
+      cap < 0 || (cap > 0 && !job))
+    return ATTN_ERR_INVALID_ARG;
+  const int n_qtiles = (N_q + 127) / 128, n_kvtiles = (N_kv + 127) / 128;
+  *n = bwd_kv_order(B * Hkv, n_kvtiles, n_qtiles, Hq / Hkv, causal ? 1 : 0, N_kv - N_q, n_sm, job,
+                    cap);
+  return ATTN_OK;
+}
+
 int attn_selftest_timeout(int limit_us, attn_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
   const int dev_ok = check_device();

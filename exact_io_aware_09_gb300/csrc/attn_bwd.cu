@@ -922,23 +922,14 @@ static int kv_job_steps(int kt, int n_qtiles, int G, int causal, int off) {
   return nq_per > 0 ? 2 * G * nq_per : 0;
 }
 
-// The packed dispatch order (KvOrder) for one shape, computed once and kept.
-static const KvOrder* kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal,
-                               int off) {
-  static const KvOrder kDefault = {0, {}};
-  const int n_jobs = n_planes * n_kvtiles;
-  int dev = 0, n_sm = 0;
-  if (!causal || n_jobs > kMaxKvOrder || cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      n_sm <= 0 || n_jobs <= n_sm)
-    return &kDefault;
-  using Key = std::tuple<int, int, int, int, int, int>;
-  static std::map<Key, std::unique_ptr<KvOrder>> cache;
-  static std::mutex mu;
-  const Key key{n_planes, n_kvtiles, n_qtiles, G, off, n_sm};
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second.get();
+// The packed dispatch order for a grid of n_planes x n_kvtiles jobs on n_sm SMs: writes the job
+// of every block to job[0 .. n) and returns n, or 0 when the default order stands (no causal
+// mask: equal jobs; no more jobs than SMs; more than `cap` jobs).
+int bwd_kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal, int off, int n_sm,
+                 uint16_t* job, int cap) {
+  const long long n_jobs_ll = static_cast<long long>(n_planes) * n_kvtiles;
+  if (!causal || n_sm <= 0 || n_jobs_ll <= n_sm || n_jobs_ll > cap || n_jobs_ll > 65536) return 0;
+  const int n_jobs = static_cast<int>(n_jobs_ll);
   // job weights: its steps plus a block's fixed cost (about four steps: setup, K/V load,
   // pipeline fill, dK/dV store)
   std::vector<long long> w(n_jobs);
@@ -950,22 +941,33 @@ static const KvOrder* kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G,
   std::vector<int> by_size(n_jobs);
   for (int j = 0; j < n_jobs; ++j) by_size[j] = j;
   std::stable_sort(by_size.begin(), by_size.end(), [&](int x, int y) { return w[x] > w[y]; });
-  const long long cap = (total + n_sm - 1) / n_sm;
-  std::vector<std::vector<int>> bins(n_sm);
-  std::vector<long long> load(n_sm, 0);
-  for (int j : by_size) {
-    int best = -1, emptiest = 0;
-    for (int b = 0; b < n_sm; ++b) {
-      if (load[b] + w[j] <= cap && (best < 0 || load[b] > load[best])) best = b;
-      if (load[b] < load[emptiest]) emptiest = b;
+  // best fit under a cap a little above the average load; of a few caps, the plan whose
+  // fullest bin is lowest
+  const long long avg = (total + n_sm - 1) / n_sm;
+  std::vector<std::vector<int>> bins;
+  long long best_max = -1;
+  for (int step = 0; step <= 12; ++step) {
+    const long long bin_cap = avg + avg * step / 400;  // up to 3% above the average
+    std::vector<std::vector<int>> trial(n_sm);
+    std::vector<long long> load(n_sm, 0);
+    for (int j : by_size) {
+      int best = -1, emptiest = 0;
+      for (int b = 0; b < n_sm; ++b) {
+        if (load[b] + w[j] <= bin_cap && (best < 0 || load[b] > load[best])) best = b;
+        if (load[b] < load[emptiest]) emptiest = b;
+      }
+      const int b = best >= 0 ? best : emptiest;
+      trial[b].push_back(j);  // largest first within a bin
+      load[b] += w[j];
     }
-    const int b = best >= 0 ? best : emptiest;
-    bins[b].push_back(j);  // largest first within a bin
-    load[b] += w[j];
+    const long long mx = *std::max_element(load.begin(), load.end());
+    if (best_max < 0 || mx < best_max) {
+      best_max = mx;
+      bins.swap(trial);
+    }
   }
   // the order in which SMs that free up in turn take the bins' jobs
-  auto order = std::make_unique<KvOrder>();
-  order->n = 0;
+  int n = 0;
   using Slot = std::pair<long long, int>;  // (time the SM frees up, bin)
   std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
   std::vector<size_t> next(n_sm, 0);
@@ -976,11 +978,32 @@ static const KvOrder* kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G,
     const int b = sl.second;
     if (next[b] < bins[b].size()) {
       const int j = bins[b][next[b]++];
-      order->job[order->n++] = static_cast<uint16_t>(j);
+      job[n++] = static_cast<uint16_t>(j);
       free_at.push({sl.first + w[j], b});
     }
   }
-  if (order->n != n_jobs) return &kDefault;
+  return n == n_jobs ? n : 0;
+}
+
+// The packed dispatch order (KvOrder) for one shape on the current device, computed once and
+// kept.
+static const KvOrder* kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal,
+                               int off) {
+  static const KvOrder kDefault = {0, {}};
+  int dev = 0, n_sm = 0;
+  if (!causal || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return &kDefault;
+  using Key = std::tuple<int, int, int, int, int, int>;
+  static std::map<Key, std::unique_ptr<KvOrder>> cache;
+  static std::mutex mu;
+  const Key key{n_planes, n_kvtiles, n_qtiles, G, off, n_sm};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second.get();
+  auto order = std::make_unique<KvOrder>();
+  order->n = bwd_kv_order(n_planes, n_kvtiles, n_qtiles, G, causal, off, n_sm, order->job,
+                          kMaxKvOrder);
   const KvOrder* out = order.get();
   cache.emplace(key, std::move(order));
   return out;

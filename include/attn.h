@@ -329,6 +329,25 @@ int attn_fwd_kv_span(int q_tile, int block_m, int block_n, int N_q, int N_kv, in
                      int window, int *j_begin, int *j_end, int *lo_masked, int *hi_masked);
 
 /*
+ * attn_bwd_kv_order -- host-side copy of the order in which attn_bwd launches the blocks of its
+ * dK/dV kernel (one block per 128-key tile of each (batch, key/value head)), exposed so the
+ * schedule can be checked without a GPU.  Under the causal mask a block's work grows with the
+ * query tiles that see its key tile; the blocks are packed into one bin per SM (largest first,
+ * each into the fullest bin that stays under the average load) and listed in the order in which
+ * SMs that free up in turn would take them.  Jobs are numbered key tile major:
+ * job = key_tile * (B * Hkv) + b * Hkv + h.
+ *
+ *   n_sm   SMs the grid runs on
+ *   job    [cap] out: the job of launch block i, i < *n
+ *   *n     entries written; 0 when the launch keeps the default order (job = block index: no
+ *          causal mask, no more blocks than SMs, or more than `cap` blocks; attn_bwd itself
+ *          uses cap = 2048)
+ * Returns ATTN_OK or ATTN_ERR_INVALID_ARG.
+ */
+int attn_bwd_kv_order(int B, int Hq, int Hkv, int N_q, int N_kv, int causal, int n_sm,
+                      uint16_t *job, int cap, int *n);
+
+/*
  * attn_selftest_timeout -- launch one tiny kernel that waits on a barrier nothing ever
  * arrives at, with a limit of `limit_us` microseconds (1 .. 1000000), then records
  * ATTN_ERR_TIMEOUT in the status word and returns.  Used to check, on a GPU, that a wait which

@@ -214,3 +214,52 @@ def test_kv_span_covers_exactly_the_visible_keys(attn, causal, window):
                     assert not (jb <= j < je) or j == jb or j == je - 1, (qt, j, jb, je)
                 if max(jb, lo) <= j < hi:
                     assert tile.shape[1] == bn and tile.all(), (N_q, N_kv, qt, j, lo, hi)
+
+
+def _list_schedule(order, weights, n_sm):
+    """Makespan of blocks taken in `order` by whichever of n_sm SMs frees up first."""
+    import heapq
+
+    free = [(0, i) for i in range(n_sm)]
+    heapq.heapify(free)
+    end = 0
+    for j in order:
+        t, i = heapq.heappop(free)
+        t += weights[j]
+        end = max(end, t)
+        heapq.heappush(free, (t, i))
+    return end
+
+
+def test_bwd_kv_order_packs_the_causal_grid(attn):
+    """The 8192-token GQA backward (B=1, Hq=64, Hkv=8) on 152 SMs: every job exactly once, and
+    taken in that order by the SMs as they free up the blocks finish within 1% of the average
+    load, against about 7% over it when started longest first."""
+    B, Hq, Hkv, N, n_sm = 1, 64, 8, 8192, 152
+    order = attn.attn_bwd_kv_order(B, Hq, Hkv, N, N, True, n_sm)
+    n_planes, n_kt = B * Hkv, N // 128
+    assert sorted(order) == list(range(n_planes * n_kt))
+    # a job's 64-query steps under the causal mask, plus the block's fixed cost (4)
+    weights = [2 * (Hq // Hkv) * (N // 128 - j // n_planes) + 4 for j in range(n_planes * n_kt)]
+    avg = sum(weights) / n_sm
+    packed = _list_schedule(order, weights, n_sm)
+    longest_first = _list_schedule(range(n_planes * n_kt), weights, n_sm)
+    assert packed <= 1.01 * avg, (packed, avg)
+    assert longest_first > 1.05 * avg  # the tail the packing removes
+    assert packed < longest_first
+
+
+def test_bwd_kv_order_keeps_the_default_order(attn):
+    # equal jobs (no causal mask), no more blocks than SMs, more blocks than the table holds
+    assert attn.attn_bwd_kv_order(1, 64, 8, 8192, 8192, False, 152) == []
+    assert attn.attn_bwd_kv_order(1, 16, 2, 1024, 1024, True, 152) == []
+    assert attn.attn_bwd_kv_order(8, 64, 8, 8192, 8192, True, 152, cap=2048) == []
+    with pytest.raises(attn.AttnError):
+        attn.attn_bwd_kv_order(1, 6, 4, 128, 128, True, 152)  # Hq not a multiple of Hkv
+
+
+def test_bwd_kv_order_bottom_right_alignment(attn):
+    """N_kv > N_q (bottom-right causal alignment): still a permutation of the jobs."""
+    B, Hq, Hkv, Nq, Nkv = 2, 16, 8, 3000, 9000
+    order = attn.attn_bwd_kv_order(B, Hq, Hkv, Nq, Nkv, True, 152)
+    assert sorted(order) == list(range(B * Hkv * (-(-Nkv // 128))))
