@@ -127,6 +127,11 @@ __global__ void selftest_timeout_kernel(int* status, uint64_t limit_ns) {
   wait_bounded(smem_u32(&bar), 0, nullptr, status, limit_ns);
 }
 
+// Dispatch order of the dK/dV kernel's blocks (attn_bwd.cu): job of every block in job[0 .. n),
+// n returned; 0 = the default order.
+int bwd_kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal, int off, int n_sm,
+                 uint16_t* job, int cap);
+
 }  // namespace attn
 
 using namespace attn;

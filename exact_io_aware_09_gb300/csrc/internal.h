@@ -160,10 +160,6 @@ size_t fp8_workspace_layout(int B, int Hq, int Hkv, int N_q, int N_kv, int d, si
 int launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
 int launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int Hq, int N_q);
-// Dispatch order of the dK/dV kernel's blocks (see attn_bwd.cu): job of every block in
-// job[0 .. n), n returned; 0 = the default order.
-int bwd_kv_order(int n_planes, int n_kvtiles, int n_qtiles, int G, int causal, int off, int n_sm,
-                 uint16_t* job, int cap);
 size_t decode_workspace_bytes(int B, int Hq, int max_seqlen, int split, int d);
 // Device address and size of the library-owned decode scratch of the current device
 // (set up on the first call per device).  Returns 0 or an attn_status_t value.
