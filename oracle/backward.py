@@ -22,29 +22,45 @@ gradients of one key/value head are the sums over its query heads.  Masks are th
 forward oracle (causal bottom-right aligned; a row with no visible key has P = 0 and
 contributes nothing).  numpy's matmul is the only library step.
 """
+from collections import namedtuple
+
 import numpy as np
 
 from . import bits_to_double, round_to_storage
 
+GradScales = namedtuple("GradScales", ["row", "elem", "given_row", "given_elem"])
+GradScales.__doc__ = """Rounding scales of the gradients for one unit of the storage type.
+row: (eq [..,Nq], ek, ev [..,Nkv]), bounds on the L2 error of each gradient row, and
+elem: (eq, ek, ev) with the gradients' own shapes, bounds on each element's error, for a
+kernel that forms D from O as a forward kernel stored it; given_row, given_elem: the same
+for a kernel handed the oracle's own stored O (and L), so that only fp32 sums separate the
+two D's."""
 
-def _head_backward(q, k, v, do, causal, scale, window=None, stored_dtype=None, unit=None):
+
+def _head_backward(q, k, v, do, causal, scale, window=None, stored_dtype=None, unit=None,
+                   tiny=0.0):
     """One head, fp64 arrays q [Nq, d], k/v [Nkv, d], do [Nq, d] -> (dq, dk, dv, o, lse).
     stored_dtype: round O to this storage type before forming D (None: exact O).
-    unit: if given, also return per-row rounding scales (see below) for this unit roundoff."""
+    unit: if given, also return the rounding scales described below for this unit roundoff
+    (one ulp at 1 of the storage type); tiny is that type's subnormal spacing."""
     Nq, Nkv = q.shape[0], k.shape[0]
     s = scale * (q @ k.T)
+    i = np.arange(Nq)[:, None] + (Nkv - Nq)
+    j = np.arange(Nkv)[None, :]
+    vis = np.ones((Nq, Nkv), dtype=bool)
     if causal or window is not None:
-        i = np.arange(Nq)[:, None] + (Nkv - Nq)
-        j = np.arange(Nkv)[None, :]
         vis = j <= i
         if window is not None:
             vis &= (i - j) <= window
         s = np.where(vis, s, -np.inf)
     m = s.max(axis=1, keepdims=True) if Nkv else np.full((Nq, 1), -np.inf)
     live = np.isfinite(m[:, 0])
+    vis &= live[:, None]
     e = np.where(live[:, None], np.exp(s - np.where(live[:, None], m, 0.0)), 0.0)
+    del s
     l = e.sum(axis=1, keepdims=True)
     p = np.where(live[:, None], e / np.where(l > 0, l, 1.0), 0.0)
+    del e
     o = p @ v
     lse = np.where(live, m[:, 0] + np.log(np.where(l[:, 0] > 0, l[:, 0], 1.0)), -np.inf)
     dv = p.T @ do
@@ -53,22 +69,55 @@ def _head_backward(q, k, v, do, causal, scale, window=None, stored_dtype=None, u
                                                             stored_dtype)
     D = (do * o_used).sum(axis=1, keepdims=True)
     ds = p * (dp - D)
+    del dp
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)
     if unit is None:
         return dq, dk, dv, o, lse
     # Rounding scales of a kernel that follows the pages' algorithm: P and dS rounded to the
-    # storage type before their products (relative `unit` per term), and D formed from a stored O
-    # that may differ from the exact one by one unit of the storage type in each element
-    # (|dD_i| <= unit * sum_c |dO_ic O_ic|; dS moves by -P dD, i.e. dQ_i by -scale dD_i (P K)_i).
+    # storage type before their products, each rounding bounded by `unit` times the rounded
+    # value plus `tiny` (the subnormal spacing of fp16; negligible for bf16), and D formed from a
+    # stored O that differs from the oracle's by dO_stored, which moves D_i by
+    # dd_i = sum_c |dO_ic| |dO_stored_ic|.  A rounded dS_ij (or P_ij) moves each output element
+    # by its own term: dQ_ic by scale |K_jc| (unit |dS_ij| + tiny), dK_jc by
+    # scale |Q_ic| (unit |dS_ij| + tiny), dV_jc by |dO_ic| (unit P_ij + tiny).  The D error
+    # moves the whole row of dS by -P_i dD_i: dQ_i by exactly -scale dD_i (P K)_i, and dK_j by
+    # scale sum_i P_ij dD_i Q_i, whose terms' signs are unknown.  Per row the same terms are
+    # taken with the L2 norms of the rows of K, Q and dO.
+    ads = np.abs(ds)
+    del ds
+    aq, ak, av, ado = np.abs(q), np.abs(k), np.abs(v), np.abs(do)
+    visf = vis.astype(np.float64)
+    pk = p @ k
     nk = np.linalg.norm(k, axis=1)
     nq = np.linalg.norm(q, axis=1)
     ndo = np.linalg.norm(do, axis=1)
-    dd = unit * np.abs(do * o).sum(axis=1)
-    eq = scale * (unit * (np.abs(ds) @ nk) + dd * np.linalg.norm(p @ k, axis=1))
-    ek = scale * (unit * (np.abs(ds).T @ nq) + p.T @ (dd * nq))
+    row_q = scale * unit * (ads @ nk)
+    row_k = scale * unit * (ads.T @ nq)
     ev = unit * (p.T @ ndo)
-    return dq, dk, dv, o, lse, (eq, ek, ev)
+    w = unit * ads + tiny * visf                         # per-term rounding of dS
+    del ads
+    el_q = scale * (w @ ak)
+    el_k = scale * (w.T @ aq)
+    del w
+    ev_e = (unit * p + tiny * visf).T @ ado
+
+    def with_d_term(dd_row, dd_el):
+        return ((row_q + scale * dd_row * np.linalg.norm(pk, axis=1),
+                 row_k + scale * (p.T @ (dd_row * nq)), ev),
+                (el_q + scale * dd_el[:, None] * np.abs(pk),
+                 el_k + scale * (p.T @ (dd_el[:, None] * aq)), ev_e))
+
+    # O stored by a forward kernel: one unit of its own rounding of O, one of the oracle's, and
+    # the forward's rounding of P before P V (|dO_stored| <= unit |O| + unit (P|V|) +
+    # tiny (vis|V|) + tiny per element).  The per-row scales keep the plain one-unit form.
+    o_err = unit * (np.abs(o) + p @ av) + tiny * (visf @ av + 1.0)
+    row, elem = with_d_term(unit * np.abs(do * o).sum(axis=1), (ado * o_err).sum(axis=1))
+    # O handed to the kernel by the oracle (its own rounding of the exact O): D then differs by
+    # the kernel's fp32 sum of d products only, allowed 2^-20 of sum_c |dO_ic O_ic|.
+    dd_given = 2.0 ** -20 * np.abs(do * o_used).sum(axis=1)
+    given_row, given_elem = with_d_term(dd_given, dd_given)
+    return dq, dk, dv, o, lse, GradScales(row, elem, given_row, given_elem)
 
 
 def attention_backward(q, k, v, do, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale,
@@ -80,9 +129,11 @@ def attention_backward(q, k, v, do, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale
     and dV then hold only those query heads' contributions).
     exact_o: form D from the exact fp64 O (the exact gradient) instead of O rounded to the
     storage type as the forward saves it.
-    error_scales: also return (eq [B,Hq,Nq], ek, ev [B,Hkv,Nkv]), per-row rounding scales of a
-    kernel that rounds P and dS to the storage type and forms D from a stored O that may differ
-    from the exact one by a unit of the storage type (unit = one ulp at 1: 2^-7 bf16, 2^-10 f16).
+    error_scales: also return a GradScales: rounding scales of a kernel that rounds P and dS
+    to the storage type (unit = one ulp at 1: 2^-7 bf16, 2^-10 f16; tiny = the subnormal
+    spacing, 2^-24 f16), per row ([B,Hq,Nq] for dq, [B,Hkv,Nkv] for dk, dv) and per element
+    (the gradients' shapes), for D formed from O as a forward kernel stored it (row, elem) and
+    from the oracle's own stored O handed to the kernel (given_row, given_elem).
     Returns dq [B, Hq, Nq, d], dk, dv [B, Hkv, Nkv, d], o [B, Hq, Nq, d], lse [B, Hq, Nq]
     (float64; entries of heads not computed are NaN for dq/o/lse).
     """
@@ -96,24 +147,33 @@ def attention_backward(q, k, v, do, dtype, B, Hq, Hkv, Nq, Nkv, d, causal, scale
     lse = np.full((B, Hq, Nq), np.nan)
     dk = np.zeros((B, Hkv, Nkv, d))
     dv = np.zeros((B, Hkv, Nkv, d))
-    unit = (2.0 ** -7 if str(dtype).lower().startswith("b") else 2.0 ** -10) if error_scales else None
-    eq = np.full((B, Hq, Nq), np.nan)
-    ek = np.zeros((B, Hkv, Nkv))
-    ev = np.zeros((B, Hkv, Nkv))
+    unit, tiny = storage_unit(dtype) if error_scales else (None, 0.0)
+    shapes = ((B, Hq, Nq), (B, Hkv, Nkv), (B, Hkv, Nkv))
+    acc = {f: [np.full(sh, np.nan) if n == 0 else np.zeros(sh)
+               for n, sh in enumerate(shapes if "row" in f else [x + (d,) for x in shapes])]
+           for f in GradScales._fields}
     todo = range(B * Hq) if heads is None else heads
     for bh in todo:
         b, h = divmod(int(bh), Hq)
         hk = h // G
         res = _head_backward(qd[b, h], kd[b, hk], vd[b, hk], dod[b, h], causal, scale, window,
-                             None if exact_o else dtype, unit)
+                             None if exact_o else dtype, unit, tiny)
         gq, gk, gv, go, gl = res[:5]
         dq[b, h], o[b, h], lse[b, h] = gq, go, gl
         dk[b, hk] += gk
         dv[b, hk] += gv
         if error_scales:
-            eq[b, h] = res[5][0]
-            ek[b, hk] += res[5][1]
-            ev[b, hk] += res[5][2]
+            for f, (sq, sk, sv) in zip(GradScales._fields, res[5]):
+                acc[f][0][b, h] = sq
+                acc[f][1][b, hk] += sk
+                acc[f][2][b, hk] += sv
     if error_scales:
-        return dq, dk, dv, o, lse, (eq, ek, ev)
+        return dq, dk, dv, o, lse, GradScales(*(tuple(acc[f]) for f in GradScales._fields))
     return dq, dk, dv, o, lse
+
+
+def storage_unit(dtype):
+    """(unit, tiny) of a 16-bit storage type: its ulp at 1 and its subnormal spacing."""
+    if str(dtype).lower().startswith("b"):
+        return 2.0 ** -7, 2.0 ** -133
+    return 2.0 ** -10, 2.0 ** -24

@@ -65,7 +65,7 @@ def test_decode_cases(attn, case):
     og, lg, st = run_decode(attn, dt, q, kc, vc, cu, max(lengths), split)
     assert st == 0
     orf, lrf = oracle.decode_rows(q, kc, vc, cu, dt, cfg.B, Hq, Hkv, d, cfg.scale)
-    check_rows(og, lg, orf, lrf, f"decode {case}")
+    check_rows(og, lg, orf, lrf, f"decode {case}", dtype=dt)
 
 
 def test_garbage_in_unowned_cache_rows(attn):
@@ -111,4 +111,4 @@ def test_splitkv_workload_full(attn):
     q, kc, vc = (syn.tensor_to_bits(t) for t in (qd, kd, vd))
     del kd, vd
     orf, lrf = oracle.decode_rows(q, kc, vc, cu, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.scale)
-    check_rows(og, lg, orf, lrf, cfg.name)
+    check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)

@@ -68,7 +68,7 @@ def test_window(attn, shape, W):
     og, lg = _host(o, lse, cfg.d)
     orf, lrf = oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q,
                                      cfg.N_kv, cfg.d, True, cfg.scale, window=W)
-    check_rows(og, lg, orf, lrf, f"window {W} {shape}")
+    check_rows(og, lg, orf, lrf, f"window {W} {shape}", dtype=cfg.dtype)
 
 
 def test_window_matches_causal_when_wide(attn):
@@ -95,7 +95,7 @@ def test_window_pages_example_full_size(attn):
     og, lg = _host(o, lse, cfg.d)
     orf, lrf = oracle.attention_rows(q, k, v, "bf16", 1, 64, 8, 8192, 8192, 128, True,
                                      cfg.scale, None, window=1024)
-    check_rows(og, lg, orf, lrf, "window 1024 at 8192")
+    check_rows(og, lg, orf, lrf, "window 1024 at 8192", dtype=cfg.dtype)
 
 
 BLOCK_CASES = [
@@ -128,7 +128,8 @@ def test_block_sparse(attn, shape, causal, density):
     orf, lrf = oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q,
                                      cfg.N_kv, cfg.d, causal, cfg.scale, block_mask=mask,
                                      block=128)
-    check_rows(og, lg, orf, lrf, f"block-sparse {shape} causal={causal}")
+    check_rows(og, lg, orf, lrf, f"block-sparse {shape} causal={causal}",
+               dtype=cfg.dtype)
 
 
 def test_block_sparse_all_ones_is_dense(attn):

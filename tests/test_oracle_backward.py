@@ -112,22 +112,117 @@ def test_stored_output_changes_only_the_d_term():
     assert np.abs(oracle.bits_to_double(o_bits, BF16) - ex[3]).max() <= 2.0 ** -8 * np.abs(ex[3]).max()
 
 
+def _head(dtype, causal, seed, Nq=300, Nkv=300, d=64):
+    from oracle.backward import _head_backward, storage_unit
+
+    cfg, q, k, v, do = _inputs(1, 1, 1, Nq, Nkv, d, seed, dtype, causal)
+    qd, kd, vd, dod = (oracle.bits_to_double(x, dtype).reshape(-1, d) for x in (q, k, v, do))
+    unit, tiny = storage_unit(dtype)
+    res = _head_backward(qd, kd, vd, dod, causal, cfg.scale, stored_dtype=dtype, unit=unit,
+                         tiny=tiny)
+    return cfg, (qd, kd, vd, dod), res
+
+
+def _rnd(x, dtype):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    return oracle.bits_to_double(oracle.round_to_storage(x, dtype), dtype)
+
+
+def _kernel_like_gradients(qd, kd, vd, dod, causal, scale, dtype, given=None):
+    """The pages' forward and backward with every rounding a 16-bit kernel makes, in fp64
+    otherwise: P unnormalised and rounded before P V, O rounded, L = m + ln l (or O and L as
+    given); then P from L, D from the stored O, P and dS rounded before their products, the
+    gradients rounded."""
+    Nq, Nkv = qd.shape[0], kd.shape[0]
+    s = scale * (qd @ kd.T)
+    if causal:
+        s = np.where(np.arange(Nkv)[None, :] <= np.arange(Nq)[:, None] + (Nkv - Nq), s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    live = np.isfinite(m)
+    if given is None:
+        pt = np.where(live, np.exp(s - np.where(live, m, 0.0)), 0.0)
+        lsum = pt.sum(axis=1, keepdims=True)
+        o = _rnd(np.where(live, (_rnd(pt, dtype) @ vd) / np.where(live, lsum, 1.0), 0.0), dtype)
+        L = np.where(live, m + np.log(np.where(live, lsum, 1.0)), -np.inf)
+    else:
+        o, L = given
+        L = L.astype(np.float32).astype(np.float64)[:, None]
+    p = np.where(live, np.exp(s - np.where(live, L, 0.0)), 0.0)
+    ds = p * (dod @ vd.T - (dod * o).sum(axis=1, keepdims=True))
+    dv = _rnd(_rnd(p, dtype).T @ dod, dtype)
+    dsr = _rnd(ds, dtype)
+    return _rnd(scale * (dsr @ kd), dtype), _rnd(scale * (dsr.T @ qd), dtype), dv
+
+
+@pytest.mark.parametrize("given", [False, True], ids=["forward_o", "oracle_o"])
+@pytest.mark.parametrize("dtype,causal", [(BF16, True), (F16, True), (BF16, False), (F16, False)])
+def test_gradient_bounds_hold_for_a_kernel_with_the_pages_roundings(dtype, causal, given):
+    """The row and element bounds of the GPU parity check contain the gradients of a model of
+    the kernel's arithmetic (every rounding to 16 bits it makes, fp64 elsewhere), for D formed
+    from a forward kernel's stored O and from the oracle's stored O handed over: the bounds are
+    not tighter than the rounding they describe."""
+    from parity import grad_violations
+
+    cfg, (qd, kd, vd, dod), res = _head(dtype, causal, 97 + causal, 260, 300, 64)
+    o_given = _rnd(res[3], dtype)
+    got = _kernel_like_gradients(qd, kd, vd, dod, causal, cfg.scale, dtype,
+                                 (o_given, res[4]) if given else None)
+    sc = res[5]
+    rows, elems = (sc.given_row, sc.given_elem) if given else (sc.row, sc.elem)
+    for g, ref, er, ee in zip(got, res[:3], rows, elems):
+        r_row, r_el = grad_violations(g, ref, er, ee, dtype)
+        assert r_row.max() <= 1.0 and r_el.max() <= 1.0, (r_row.max(), r_el.max())
+        assert r_el.max() > 1e-3            # the model does round: the errors are not zero
+
+
+@pytest.mark.parametrize("given", [False, True], ids=["forward_o", "oracle_o"])
+def test_element_bound_catches_what_the_row_bound_lets_through(given):
+    """One corrupted element of dQ, and one corrupted channel of dQ, dK and dV across every
+    row, each half as large as the row bound allows: the row check passes all of them, the
+    element check fails them.  With D from a forward kernel's O the element bound of dK holds
+    the worst case of the forward's P rounding, so it catches most corrupted rows, not all."""
+    from parity import GRAD_FLOOR, GRAD_RTOL_ROW, GRAD_SCALE_FACTOR, grad_violations
+
+    cfg, _, (dq, dk, dv, o, lse, sc) = _head(BF16, True, 95)
+    rows, elems = (sc.given_row, sc.given_elem) if given else (sc.row, sc.elem)
+
+    def row_allow(ref, e):
+        return GRAD_SCALE_FACTOR * e + GRAD_RTOL_ROW * np.linalg.norm(ref, axis=1) + GRAD_FLOOR
+
+    # one element
+    bad = dq.copy()
+    r, c = 217, 13
+    bad[r, c] += 0.5 * row_allow(dq, rows[0])[r]
+    r_row, r_el = grad_violations(bad, dq, rows[0], elems[0], BF16)
+    assert r_row.max() <= 1.0 and r_el.max() > 1.0, (r_row.max(), r_el.max())
+    # one channel of every row (key rows that no query sees have a zero gradient and bound)
+    for which, g, c in ((0, dq, 3), (1, dk, 40), (2, dv, 5)):
+        bad = g.copy()
+        bad[:, c] -= 0.5 * row_allow(g, rows[which])
+        r_row, r_el = grad_violations(bad, g, rows[which], elems[which], BF16)
+        live = np.abs(g).sum(axis=1) > 0
+        caught = (r_el[live, c] > 1.0).mean()
+        assert r_row.max() <= 1.0 and caught >= (0.8 if which == 1 and not given else 1.0), \
+            (which, r_row.max(), caught)
+
+
 def test_gradient_tolerance_rejects_plausible_mistakes():
-    """The per-row bound used by the GPU parity test (2 x the rounding scales + 1% of the row
-    norm) separates a correct gradient from one with a dropped D term, a missing scale, a
-    transposed dS or a sign error, all planted here in a copy of the oracle's arithmetic."""
-    from oracle.backward import _head_backward
+    """The bounds used by the GPU parity test (row and element checks, D from a forward
+    kernel's O or from the oracle's) separate a correct gradient from one with a dropped D
+    term, a missing scale, a transposed dS or a sign error, all planted here in a copy of the
+    oracle's arithmetic."""
+    from parity import grad_violations
 
-    cfg, q, k, v, do = _inputs(1, 1, 1, 300, 300, 64, 95, BF16, True)
-    qd, kd, vd, dod = (oracle.bits_to_double(x, BF16).reshape(300, 64) for x in (q, k, v, do))
-    dq, dk, dv, o, lse, (eq, ek, ev) = _head_backward(qd, kd, vd, dod, True, cfg.scale,
-                                                      stored_dtype=BF16, unit=2.0 ** -7)
+    cfg, (qd, kd, vd, dod), (dq, dk, dv, o, lse, sc) = _head(BF16, True, 95)
 
-    def passes(got, ref, scales):
-        err = np.linalg.norm(got - ref, axis=1)
-        return bool(np.all(err <= 2.0 * scales + 1e-2 * np.linalg.norm(ref, axis=1) + 1e-6))
+    def passes(got, ref, which):
+        for rows, elems in ((sc.row, sc.elem), (sc.given_row, sc.given_elem)):
+            r_row, r_el = grad_violations(got, ref, rows[which], elems[which], BF16)
+            if r_row.max() > 1.0 or r_el.max() > 1.0:
+                return False
+        return True
 
-    assert passes(dq, dq, eq) and passes(dk, dk, ek) and passes(dv, dv, ev)
+    assert passes(dq, dq, 0) and passes(dk, dk, 1) and passes(dv, dv, 2)
     # the same algebra with one planted mistake each
     s = cfg.scale * (qd @ kd.T)
     i = np.arange(300)[:, None]
@@ -136,8 +231,8 @@ def test_gradient_tolerance_rejects_plausible_mistakes():
     p /= p.sum(axis=1, keepdims=True)
     dp = dod @ vd.T
     D = (dod * o).sum(axis=1, keepdims=True)
-    assert not passes(cfg.scale * ((p * dp) @ kd), dq, eq)                    # D dropped
-    assert not passes((p * (dp - D)) @ kd, dq, eq)                             # scale missing
-    assert not passes(cfg.scale * ((p * (D - dp)) @ kd), dq, eq)               # sign of dS
-    assert not passes(cfg.scale * ((p * (dp - D)) @ qd), dk, ek)               # dS not transposed
-    assert not passes(p @ dod, dv, ev)                                         # P instead of P^T
+    assert not passes(cfg.scale * ((p * dp) @ kd), dq, 0)                    # D dropped
+    assert not passes((p * (dp - D)) @ kd, dq, 0)                             # scale missing
+    assert not passes(cfg.scale * ((p * (D - dp)) @ kd), dq, 0)               # sign of dS
+    assert not passes(cfg.scale * ((p * (dp - D)) @ qd), dk, 1)               # dS not transposed
+    assert not passes(p @ dod, dv, 2)                                         # P instead of P^T

@@ -49,7 +49,7 @@ def test_paged_decode_vs_oracle(attn, page_size, d, dtype, Hq, Hkv):
     lg = lse.cpu().numpy().astype(np.float64).reshape(-1)
     orf, lrf = oracle.decode_rows_paged(q, kp, vp, table, LENGTHS, page_size, dtype, cfg.B, Hq,
                                         Hkv, d, cfg.scale)
-    check_rows(og, lg, orf, lrf, f"paged decode page={page_size} d={d}")
+    check_rows(og, lg, orf, lrf, f"paged decode page={page_size} d={d}", dtype=dtype)
 
 
 def test_paged_full_workload_equals_packed(attn):

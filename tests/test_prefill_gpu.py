@@ -78,7 +78,7 @@ def test_small_shapes(attn, shape):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, f"shape {shape}")
+    check_rows(og, lg, orf, lrf, f"shape {shape}", dtype=dt)
 
 
 @pytest.mark.parametrize("shape", MANY_ITEMS, ids=lambda s: "x".join(map(str, s)))
@@ -88,7 +88,7 @@ def test_many_items(attn, shape):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, f"shape {shape}")
+    check_rows(og, lg, orf, lrf, f"shape {shape}", dtype=dt)
 
 
 def test_output_16_byte_aligned(attn):
@@ -107,7 +107,7 @@ def test_output_16_byte_aligned(attn):
     og = o.float().cpu().numpy().astype(np.float64).reshape(-1, cfg.d)
     lg = lse.cpu().numpy().astype(np.float64).reshape(-1)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, "16-byte aligned O")
+    check_rows(og, lg, orf, lrf, "16-byte aligned O", dtype=cfg.dtype)
 
 
 def test_large_logits_small(attn):
@@ -115,7 +115,7 @@ def test_large_logits_small(attn):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, "x8 logits")
+    check_rows(og, lg, orf, lrf, "x8 logits", dtype=cfg.dtype)
 
 
 def test_no_keys_and_empty_inputs(attn):
@@ -152,7 +152,7 @@ def test_workload_full(attn, cfg):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, cfg.name)
+    check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)
 
 
 @pytest.mark.parametrize("cfg", [syn.CONFIG3A, syn.CONFIG3B, syn.CONFIG3SA, syn.CONFIG3SB],
@@ -161,7 +161,7 @@ def test_long_workload_full(attn, cfg):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, cfg.name)
+    check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)
 
 
 def test_gqa_long_context_full(attn):
@@ -171,4 +171,4 @@ def test_gqa_long_context_full(attn):
     q, k, v = cfg.host_inputs()
     og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, cfg.name)
+    check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)
