@@ -31,6 +31,9 @@ from .tiles import causal_tiles  # noqa: F401
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# A prebuilt copy of the library to load instead (the mutation check of the pins builds copies
+# of attn_oracle.c with one planted mistake each and runs the pins against them).
+_LIB_OVERRIDE = os.environ.get("ORACLE_LIB_OVERRIDE")
 _lock = threading.Lock()
 _lib = None
 _tables = {}
@@ -54,8 +57,11 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        build()
-        lib = ctypes.CDLL(_LIB)
+        if _LIB_OVERRIDE:
+            lib = ctypes.CDLL(_LIB_OVERRIDE)
+        else:
+            build()
+            lib = ctypes.CDLL(_LIB)
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_attention_rows.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
