@@ -12,10 +12,13 @@ import math
 import os
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes",
+    "AttnError", "attn_fwd", "attn_fwd_window", "attn_fwd_block_sparse", "attn_fwd_fp8",
+    "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8_workspace_offsets",
+    "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_decode_splitkv", "attn_decode_workspace_bytes", "attn_decode_paged",
     "attn_decode_splitkv_static", "attn_decode_static_scratch_bytes",
-    "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_bwd_kv_order",
-    "attn_selftest_timeout",
+    "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_fwd_kv_span",
+    "attn_bwd_kv_order", "attn_selftest_timeout",
     "attn_version", "library_path", "lib",
 ]
 
@@ -102,11 +105,29 @@ def _torch():
     return torch
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
+    """The raw handle of ``stream`` (a torch stream or an integer handle); None = torch's
+    current stream of ``device`` (of the current device when that is None too).  A torch
+    stream must belong to ``device``."""
     torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and getattr(stream, "device", device) != device:
+        raise AttnError(-1, f"stream on {stream.device}, tensors on {device}")
     return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _on_device(where, first, *others):
+    """Checks that every given tensor sits on ``first``'s CUDA device and returns a context
+    that makes that device current, so that the library's launches, its per-device state and
+    torch's default stream all refer to the device that holds the data."""
+    torch = _torch()
+    if not first.is_cuda:
+        raise AttnError(-1, f"{where}: tensors must be CUDA tensors")
+    for t in others:
+        if t is not None and t.device != first.device:
+            raise AttnError(-1, f"{where}: tensors on {first.device} and {t.device}")
+    return torch.cuda.device(first.device)
 
 
 def _dtype_code(t) -> int:
@@ -149,9 +170,10 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | Non
         lse = torch.empty((B, Hq, N_q), device=q.device, dtype=torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    st = lib.attn_fwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
-                      _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(bool(causal)),
-                      float(scale), _stream_handle(stream), _dtype_code(q))
+    with _on_device("attn_fwd", q, k, v, o, lse):
+        st = lib.attn_fwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                          _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(bool(causal)),
+                          float(scale), _stream_handle(stream, q.device), _dtype_code(q))
     _check(st, "attn_fwd")
     return o, lse
 
@@ -198,11 +220,13 @@ def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
     if workspace is None:
         workspace = torch.empty(max(int(lib.attn_bwd_workspace_bytes(B, Hq, N_q)), 1),
                                 device=q.device, dtype=torch.uint8)
-    st = lib.attn_bwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
-                      _dev_ptr(dout, "dout"), _dev_ptr(lse, "lse"), _dev_ptr(dq, "dq"),
-                      _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), B, Hq, Hkv, N_q, N_kv, d,
-                      int(bool(causal)), float(scale), _dtype_code(q),
-                      _dev_ptr(workspace, "workspace"), workspace.numel(), _stream_handle(stream))
+    with _on_device("attn_bwd", q, k, v, o, dout, lse, dq, dk, dv, workspace):
+        st = lib.attn_bwd(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                          _dev_ptr(dout, "dout"), _dev_ptr(lse, "lse"), _dev_ptr(dq, "dq"),
+                          _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), B, Hq, Hkv, N_q, N_kv, d,
+                          int(bool(causal)), float(scale), _dtype_code(q),
+                          _dev_ptr(workspace, "workspace"), workspace.numel(),
+                          _stream_handle(stream, q.device))
     _check(st, "attn_bwd")
     return dq, dk, dv
 
@@ -230,11 +254,13 @@ def attn_fwd_fp8(q, k, v, signs=None, o=None, lse=None, causal: bool = False,
     if workspace is None:
         workspace = torch.empty(max(1, attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d)),
                                 device=q.device, dtype=torch.uint8)
-    st = lib.attn_fwd_fp8(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
-                          _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(bool(causal)), scale,
-                          _dev_ptr(signs, "signs") if signs is not None else None,
-                          _dev_ptr(workspace, "workspace"), workspace.numel(),
-                          _stream_handle(stream), _dtype_code(q))
+    with _on_device("attn_fwd_fp8", q, k, v, o, lse, signs, workspace):
+        st = lib.attn_fwd_fp8(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                              _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d,
+                              int(bool(causal)), scale,
+                              _dev_ptr(signs, "signs") if signs is not None else None,
+                              _dev_ptr(workspace, "workspace"), workspace.numel(),
+                              _stream_handle(stream, q.device), _dtype_code(q))
     _check(st, "attn_fwd_fp8")
     return o, lse
 
@@ -246,9 +272,11 @@ def attn_fwd_window(q, k, v, window: int, o=None, lse=None, scale: float | None 
     Shapes and return value as attn_fwd.
     """
     B, Hq, Hkv, N_q, N_kv, d, o, lse, scale = _fwd_prep(q, k, v, o, lse, scale)
-    st = lib.attn_fwd_window(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
-                             _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d, int(window), scale,
-                             _stream_handle(stream), _dtype_code(q))
+    with _on_device("attn_fwd_window", q, k, v, o, lse):
+        st = lib.attn_fwd_window(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                 _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv, d,
+                                 int(window), scale, _stream_handle(stream, q.device),
+                                 _dtype_code(q))
     _check(st, "attn_fwd_window")
     return o, lse
 
@@ -264,10 +292,12 @@ def attn_fwd_block_sparse(q, k, v, block_mask, causal: bool = False, o=None, lse
     if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != shape
             or not block_mask.is_contiguous()):
         raise AttnError(-1, f"attn_fwd_block_sparse: block_mask must be contiguous uint8 {shape}")
-    st = lib.attn_fwd_block_sparse(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
-                                   _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q, N_kv,
-                                   d, int(bool(causal)), _dev_ptr(block_mask, "block_mask"), scale,
-                                   _stream_handle(stream), _dtype_code(q))
+    with _on_device("attn_fwd_block_sparse", q, k, v, o, lse, block_mask):
+        st = lib.attn_fwd_block_sparse(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                       _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B, Hq, Hkv, N_q,
+                                       N_kv, d, int(bool(causal)),
+                                       _dev_ptr(block_mask, "block_mask"), scale,
+                                       _stream_handle(stream, q.device), _dtype_code(q))
     _check(st, "attn_fwd_block_sparse")
     return o, lse
 
@@ -307,13 +337,16 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, max_seqlen_k:
     need = attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
-    st = lib.attn_decode_paged(_dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"),
-                               _dev_ptr(v_pages, "v_pages"), _dev_ptr(block_table, "block_table"),
-                               _dev_ptr(seqlens_k, "seqlens_k"), num_pages, page_size,
-                               block_table.shape[1], int(max_seqlen_k), _dev_ptr(o, "o"),
-                               _dev_ptr(lse, "lse"), B, Hq, Hkv, d, int(split_size), float(scale),
-                               _dtype_code(q), _dev_ptr(workspace, "workspace"),
-                               workspace.numel(), _stream_handle(stream))
+    with _on_device("attn_decode_paged", q, k_pages, v_pages, block_table, seqlens_k, o, lse,
+                    workspace):
+        st = lib.attn_decode_paged(_dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"),
+                                   _dev_ptr(v_pages, "v_pages"),
+                                   _dev_ptr(block_table, "block_table"),
+                                   _dev_ptr(seqlens_k, "seqlens_k"), num_pages, page_size,
+                                   block_table.shape[1], int(max_seqlen_k), _dev_ptr(o, "o"),
+                                   _dev_ptr(lse, "lse"), B, Hq, Hkv, d, int(split_size),
+                                   float(scale), _dtype_code(q), _dev_ptr(workspace, "workspace"),
+                                   workspace.numel(), _stream_handle(stream, q.device))
     _check(st, "attn_decode_paged")
     return o, lse
 
@@ -345,12 +378,15 @@ def attn_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, max_seqlen_k: int, o=
     need = attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
-    st = lib.attn_decode_splitkv(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
-                                 _dev_ptr(v_cache, "v_cache"), _dev_ptr(cu_seqlens_k, "cu_seqlens_k"),
-                                 cap, int(max_seqlen_k), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B,
-                                 Hq, Hkv, d, int(split_size), float(scale), _dtype_code(q),
-                                 _dev_ptr(workspace, "workspace"), workspace.numel(),
-                                 _stream_handle(stream))
+    with _on_device("attn_decode_splitkv", q, k_cache, v_cache, cu_seqlens_k, o, lse,
+                    workspace):
+        st = lib.attn_decode_splitkv(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+                                     _dev_ptr(v_cache, "v_cache"),
+                                     _dev_ptr(cu_seqlens_k, "cu_seqlens_k"), cap,
+                                     int(max_seqlen_k), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), B,
+                                     Hq, Hkv, d, int(split_size), float(scale), _dtype_code(q),
+                                     _dev_ptr(workspace, "workspace"), workspace.numel(),
+                                     _stream_handle(stream, q.device))
     _check(st, "attn_decode_splitkv")
     return o, lse
 
@@ -382,12 +418,14 @@ def attn_decode_splitkv_static(q, k_cache, v_cache, cu_seqlens_k, max_seqlen_k: 
         lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    st = lib.attn_decode_splitkv_static(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
-                                        _dev_ptr(v_cache, "v_cache"),
-                                        _dev_ptr(cu_seqlens_k, "cu_seqlens_k"), cap,
-                                        int(max_seqlen_k), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"),
-                                        B, Hq, Hkv, d, int(split_size), float(scale),
-                                        _dtype_code(q), _stream_handle(stream))
+    with _on_device("attn_decode_splitkv_static", q, k_cache, v_cache, cu_seqlens_k, o, lse):
+        st = lib.attn_decode_splitkv_static(_dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"),
+                                            _dev_ptr(v_cache, "v_cache"),
+                                            _dev_ptr(cu_seqlens_k, "cu_seqlens_k"), cap,
+                                            int(max_seqlen_k), _dev_ptr(o, "o"),
+                                            _dev_ptr(lse, "lse"), B, Hq, Hkv, d, int(split_size),
+                                            float(scale), _dtype_code(q),
+                                            _stream_handle(stream, q.device))
     _check(st, "attn_decode_splitkv_static")
     return o, lse
 

@@ -1,5 +1,6 @@
 // C ABI of libattn_gb300.so: argument checks, TMA descriptors, the device status word and the
 // timeout self-test.  The kernels live in attn_fwd.cu and attn_decode.cu.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -39,18 +40,31 @@ std::mutex g_status_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The kernels use tcgen05 and are built for sm_103a only.
-int check_device() {
+// The kernels use tcgen05 and are built for sm_103a only.  `data` (one of the call's buffers,
+// or null) must not be another GPU's memory: the launch goes to the current device, whose
+// kernels could not reach it.  Host memory the GPU can address is left to the caller.
+int check_device(const void* data) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
-  static int checked[kMaxDevices];  // 0 unknown, 1 ok, 2 not usable
+  static std::atomic<int> checked[kMaxDevices];  // 0 unknown, 1 ok, 2 not usable
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
-  if (checked[dev] == 0) {
+  int known = checked[dev].load(std::memory_order_relaxed);
+  if (known == 0) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ERR_DEVICE;
-    checked[dev] = (prop.major == 10 && prop.minor == 3) ? 1 : 2;
+    known = (prop.major == 10 && prop.minor == 3) ? 1 : 2;
+    checked[dev].store(known, std::memory_order_relaxed);
   }
-  return checked[dev] == 1 ? ATTN_OK : ATTN_ERR_DEVICE;
+  if (known != 1) return ATTN_ERR_DEVICE;
+  if (data) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, data) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (pa.type == cudaMemoryTypeDevice && pa.device != dev) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
 }
 
 }  // namespace
@@ -153,7 +167,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   if (!aligned16(q) || !aligned16(o) || !aligned16(lse) ||
       (N_kv > 0 && (!aligned16(k) || !aligned16(v))))
     return ATTN_ERR_MISALIGNED;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(q);
   if (dev_ok != ATTN_OK) return dev_ok;
   FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale,
             dtype == ATTN_BF16, window, block_mask};
@@ -214,7 +228,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
     return ATTN_ERR_MISALIGNED;
   if (!workspace || workspace_bytes < attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, N_q, N_kv, d))
     return ATTN_ERR_WORKSPACE;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(q);
   if (dev_ok != ATTN_OK) return dev_ok;
   FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N_q, N_kv, d, causal ? 1 : 0, scale,
             dtype == ATTN_BF16, -1, nullptr};
@@ -249,7 +263,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return ATTN_ERR_MISALIGNED;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(N_q > 0 ? q : k);
   if (dev_ok != ATTN_OK) return dev_ok;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (N_q == 0 || N_kv == 0) {
@@ -292,7 +306,7 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
     return ATTN_ERR_MISALIGNED;
   const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(q);
   if (dev_ok != ATTN_OK) return dev_ok;
   DecodeArgs a{q, k_cache, v_cache, cu_seqlens_k, kv_capacity, max_seqlen_k, o, lse, B,
                Hq, Hkv, d, split_size, scale, dtype == ATTN_BF16, workspace};
@@ -327,7 +341,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     return ATTN_ERR_MISALIGNED;
   const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(q);
   if (dev_ok != ATTN_OK) return dev_ok;
   DecodeArgs a{q, k_pages, v_pages, nullptr, num_pages * page_size, max_seqlen_k, o, lse, B,
                Hq, Hkv, d, split_size, scale, dtype == ATTN_BF16, workspace};
@@ -360,7 +374,7 @@ int attn_decode_splitkv_static(const void* q, const void* k_cache, const void* v
     return ATTN_ERR_MISALIGNED;
   const size_t need = decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
   if (need > attn_decode_static_scratch_bytes()) return ATTN_ERR_WORKSPACE;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(q);
   if (dev_ok != ATTN_OK) return dev_ok;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -430,7 +444,7 @@ int attn_bwd_kv_order(int B, int Hq, int Hkv, int N_q, int N_kv, int causal, int
 
 int attn_selftest_timeout(int limit_us, attn_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
-  const int dev_ok = check_device();
+  const int dev_ok = check_device(nullptr);
   if (dev_ok != ATTN_OK) return dev_ok;
   int* st = device_status_ptr();
   if (!st) return ATTN_ERR_LAUNCH;

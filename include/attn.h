@@ -13,7 +13,9 @@
  *  - Pointers named q, k, v, o, lse, k_cache, v_cache, cu_seqlens_k and workspace are DEVICE
  *    pointers into memory the caller allocated and owns.  The library allocates no device
  *    memory in any call and keeps no pointer after a call returns.
- *  - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream),
+ *    which must belong to the current device, and the buffers must be that device's memory:
+ *    a call whose q (or first buffer) lives on another GPU returns ATTN_ERR_INVALID_ARG.
  *    Calls return without synchronising.  Results are valid once the stream reaches them.
  *  - Tensors are contiguous, without strides.  Base pointers must be 16-byte aligned (the
  *    tiles are moved by the Tensor Memory Accelerator).
@@ -46,7 +48,8 @@ typedef enum {
 
 typedef enum {
     ATTN_OK = 0,
-    ATTN_ERR_INVALID_ARG = -1, /* null pointer, negative size, Hq % Hkv != 0, bad scale ... */
+    ATTN_ERR_INVALID_ARG = -1, /* null pointer, negative size, Hq % Hkv != 0, bad scale,
+                                  q in another GPU's memory than the current device ...   */
     ATTN_ERR_UNSUPPORTED = -2, /* valid request outside what the kernels implement (e.g. d)  */
     ATTN_ERR_MISALIGNED = -3,  /* a base pointer is not 16-byte aligned                       */
     ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than attn_decode_workspace_bytes */
@@ -241,15 +244,19 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
  * belongs to another allocator it has no handle to, or an embedding that lends the library only
  * its input and output buffers.  This
  * entry point takes the same inputs and outputs as attn_decode_splitkv (see there) but no
- * workspace: the partial states go to a fixed scratch array inside the library, allocated once
- * per GPU when the library is loaded and kept until the process exits.  The call itself
- * allocates nothing.
+ * workspace: the partial states go to a fixed scratch array inside the library (a file-scope
+ * __device__ array of the decode module), which the CUDA runtime places on a GPU when it loads
+ * that module there and keeps until the process exits.  With the runtime's default lazy module
+ * loading that happens at the first decode call of either kind on the device (this entry point
+ * or attn_decode_splitkv / attn_decode_paged, which share the module), so every process that
+ * decodes on a GPU holds the 32 MiB there.  No call allocates anything else.
  *
  *  - Limit: attn_decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d) must not exceed
  *    attn_decode_static_scratch_bytes() (32 MiB, e.g. 15 sequences x 64 heads x 32k tokens at
  *    512-token splits, d = 128); larger requests return ATTN_ERR_WORKSPACE before any launch.
  *  - The first call on each device looks up that device's copy of the scratch array (with the
- *    device current); make that first call before any stream capture.
+ *    device current), which may load the decode module and commit its memory; make that first
+ *    call before any stream capture.
  *  - Every call shares the one array and it keeps the last call's contents.  Nothing in it
  *    needs to start at zero, but two calls that overlap on the GPU (different streams without
  *    ordering, or two threads) race on it: order them.

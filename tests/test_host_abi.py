@@ -263,3 +263,17 @@ def test_bwd_kv_order_bottom_right_alignment(attn):
     B, Hq, Hkv, Nq, Nkv = 2, 16, 8, 3000, 9000
     order = attn.attn_bwd_kv_order(B, Hq, Hkv, Nq, Nkv, True, 152)
     assert sorted(order) == list(range(B * Hkv * (-(-Nkv // 128))))
+
+
+def test_tensors_off_the_gpu_are_refused_before_any_call():
+    """The binding checks that every tensor is a CUDA tensor on one device before it calls the
+    library (no compute runs here)."""
+    import torch
+
+    import exact_io_aware_09_gb300 as attn
+
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(attn.AttnError):
+        attn.attn_fwd(q, q, q)
+    with pytest.raises(attn.AttnError):
+        attn.attn_decode_splitkv(q[0], q[0], q[0], torch.zeros(2, dtype=torch.int32), 8)

@@ -45,6 +45,33 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
                    f"static-scratch decode {lengths}")
 
 
+def test_static_scratch_call_allocates_no_device_memory():
+    """Once the first call on the device has run, a call with preallocated o and lse takes no
+    device memory: neither torch's allocator nor the driver's free-memory count moves."""
+    import torch
+
+    import exact_io_aware_09_gb300 as attn
+
+    lengths, Hq, Hkv, d, dt = (700, 1900, 33), 16, 2, 128, "bf16"
+    cfg = syn.DecodeConfig("noalloc", len(lengths), Hq, Hkv, d, dt, 63,
+                           lengths_override=lengths)
+    q, kc, vc = cfg.host_inputs()
+    cu = torch.from_numpy(syn.cu_seqlens(lengths)).cuda()
+    qt, kt, vt = (syn.bits_to_tensor(x, dt, "cuda") for x in (q, kc, vc))
+    o = torch.empty_like(qt)
+    lse = torch.empty((len(lengths), Hq), device="cuda", dtype=torch.float32)
+    call = lambda: attn.attn_decode_splitkv_static(qt, kt, vt, cu, max(lengths), o=o, lse=lse,
+                                                   scale=cfg.scale)
+    call()
+    torch.cuda.synchronize()
+    before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+    call()
+    torch.cuda.synchronize()
+    after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+    assert attn.attn_poll_status() == 0
+    assert after == before, (before, after)
+
+
 def test_static_scratch_refuses_requests_that_do_not_fit():
     import torch
 
