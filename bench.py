@@ -369,6 +369,8 @@ def run_ours(args):
 
     # end to end through the public API with host buffers: H2D inputs, call, D2H result
     e2e = run_e2e(args, attn, pcfg, q, k, v, stream, device, world) if (do_pre and not args.no_e2e) else None
+    dec_e2e = (run_e2e_decode(args, attn, dcfg, dq, dk, dv, cu, max_len, ws, dec_bytes, stream,
+                              device, world) if (do_dec and not args.no_e2e) else None)
 
     variants = None
     if do_pre and not args.no_variants:
@@ -378,6 +380,11 @@ def run_ours(args):
         variants["decode_paged"] = measure_paged(args, attn, syn, dcfg, dq, dk, dv, do, dl, ws,
                                                  lengths, max_len, dec_bytes, stream, peaks,
                                                  peak_src)
+
+    configs = None
+    if args.only in ("both", "configs") and not args.no_configs:
+        configs = measure_configs(args, attn, syn, peaks, peak_src, device, stream,
+                                  only=args.config)
 
     cpu = None
     if rank == 0 and world == 1 and do_pre and not args.no_cpu_baseline:
@@ -434,8 +441,10 @@ def run_ours(args):
                 "frac_of_spec_8000": round(ach_b / 8000.0, 4),
                 "traffic": profiled_traffic("attn_decode_split_kernel", DEC_SOURCES),
             },
+            "e2e": dec_e2e,
         },
         "prefill_ms_per_launch": round(pre_ms / args.steps, 4),
+        "configs": configs,
         "variants": variants,
         "e2e": e2e,
         "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
@@ -448,6 +457,87 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+
+
+def causal_pairs(N_q, N_kv):
+    """Visible (query, key) pairs of one causal head (bottom-right aligned)."""
+    i = np.arange(N_q, dtype=np.int64)
+    return int(np.clip(np.minimum(i + N_kv - N_q + 1, N_kv), 0, None).sum())
+
+
+def measure_configs(args, attn, syn, peaks, peak_src, device, stream, only=None):
+    """The prefill workloads of the pages' shapes besides the headline one: the single head
+    (N=256, d=64, fp16), the GPT-2 shape (B=8, H=12, N=1024, d=64, bf16, causal), the long
+    prefill (B=4, H=32, N=4096, d=128, fp16, full and causal) and its x8-logit stress.
+
+    Each launch is timed alone with CUDA events on the launching stream, after a write of a
+    256 MB buffer (twice L2) so that no launch finds its inputs in L2; 3 warm-up launches.
+    TFLOP/s by the pages' convention (4*B*H*N^2*d, halved for causal) and by the exact count of
+    visible (query, key) pairs (4*d each); roofline against the measured bf16 dense peak (fp16
+    has the same nominal tensor rate)."""
+    import torch
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    out = {}
+    configs = [syn.CONFIG1, syn.CONFIG2, syn.CONFIG3A, syn.CONFIG3B, syn.CONFIG3SA, syn.CONFIG3SB]
+    n_launch = max(10, min(args.steps, 50))
+    for cfg in configs:
+        if only is not None and cfg.name != only:
+            continue
+        q, k, v = cfg.device_inputs(device)
+        o = torch.empty_like(q)
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.N_q), device=device, dtype=torch.float32)
+        fn = lambda: attn.attn_fwd(q, k, v, o=o, lse=lse, causal=cfg.causal, scale=cfg.scale,
+                                   stream=stream)
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_launch)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        st = attn.attn_poll_status()
+        if st != 0:
+            raise SystemExit(f"device status after {cfg.name}: {attn.attn_status_string(st)}")
+        times = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+        ms = float(np.mean(times))
+        pairs = (causal_pairs(cfg.N_q, cfg.N_kv) if cfg.causal else cfg.N_q * cfg.N_kv)
+        exact = 4.0 * cfg.d * pairs * cfg.B * cfg.Hq
+        tf = cfg.flops() / (ms / 1e3) / 1e12
+        tf_exact = exact / (ms / 1e3) / 1e12
+        out[cfg.name] = {
+            "shape": {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "N": cfg.N_q, "d": cfg.d,
+                      "dtype": cfg.dtype, "causal": cfg.causal,
+                      "q_scale": 2 ** cfg.q_scale_pow2},
+            "launches": n_launch,
+            "ms_per_launch": round(ms, 5),
+            "ms_min": round(times[0], 5),
+            "ms_median": round(times[len(times) // 2], 5),
+            "flops_per_launch": cfg.flops(),
+            "flops_exact_per_launch": exact,
+            "value": round(tf, 1),
+            "value_exact": round(tf_exact, 1),
+            "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 burst (cuBLAS); fp16 nominal rate = bf16",
+                         "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "frac_exact": round(tf_exact / peaks["bf16_tflops"], 4),
+                         "frac_of_spec_2250": round(tf / 2250.0, 4)},
+        }
+        if cfg.N_q <= 256:
+            out[cfg.name]["note"] = ("two 128-row query tiles on 152 SMs: launch- and latency-"
+                                     "bound; the time is the figure, the fraction is not meaningful")
+        del q, k, v, o, lse
+    del flush
+    return out
 
 
 def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src):
@@ -633,7 +723,29 @@ def run_e2e(args, attn, pcfg, q, k, v, stream, device, world):
     e1.record(s_out)  # the last step's result is on the host when this completes
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    (ms_max,) = reduce_max([ms], device)
+
+    # the same steps one at a time on one stream: copies in, the call, copies out
+    dq, dk, dv, do, dl = sets[0]
+
+    def serial_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        attn.attn_fwd(dq, dk, dv, o=do, lse=dl, causal=True, scale=pcfg.scale, stream=s_cmp)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    with torch.cuda.stream(s_cmp):
+        serial_step()
+        torch.cuda.synchronize()
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(s_cmp)
+        for _ in range(steps):
+            serial_step()
+        e3.record(s_cmp)
+    torch.cuda.synchronize()
+    ms_serial = e2.elapsed_time(e3)
+    ms_max, ms_serial_max = reduce_max([ms, ms_serial], device)
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = q.numel() * 2 + pcfg.B * pcfg.Hq * pcfg.N_q * 4
     return {
@@ -644,6 +756,62 @@ def run_e2e(args, attn, pcfg, q, k, v, stream, device, world):
         "steps": steps,
         "ms_per_step": round(ms_max / steps, 4),
         "pipeline": "two steps in flight: inputs up, compute and result down on three streams",
+        "serial": {
+            "value": round(pcfg.flops() * steps * world / (ms_serial_max / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "ms_per_step": round(ms_serial_max / steps, 4),
+            "pipeline": "one step at a time on one stream (copies in, call, copies out)",
+        },
+    }
+
+
+def run_e2e_decode(args, attn, dcfg, dq, dk, dv, cu, max_len, ws, dec_bytes, stream, device,
+                   world):
+    """The decode step from pinned host buffers: every step copies the new query token of every
+    sequence and the sequence offsets up, runs attn_decode_splitkv over the resident KV cache
+    (the cache is the server's state, not a per-step input) and copies O and L down; one step
+    at a time on one stream.  GB/s of the same algorithmic bytes as the device-resident line."""
+    import torch
+
+    hq = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+    hq.copy_(dq)
+    hcu = torch.empty(cu.shape, dtype=cu.dtype, pin_memory=True)
+    hcu.copy_(cu)
+    ho = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+    hl = torch.empty((dcfg.B, dcfg.Hq), dtype=torch.float32, pin_memory=True)
+    q_d, cu_d, o_d = torch.empty_like(dq), torch.empty_like(cu), torch.empty_like(dq)
+    l_d = torch.empty((dcfg.B, dcfg.Hq), device=device, dtype=torch.float32)
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        q_d.copy_(hq, non_blocking=True)
+        cu_d.copy_(hcu, non_blocking=True)
+        attn.attn_decode_splitkv(q_d, dk, dv, cu_d, max_len, o=o_d, lse=l_d,
+                                 split_size=dcfg.split, scale=dcfg.scale, workspace=ws,
+                                 stream=stream)
+        ho.copy_(o_d, non_blocking=True)
+        hl.copy_(l_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        barrier(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    (ms_max,) = reduce_max([e0.elapsed_time(e1)], device)
+    return {
+        "value": round(dec_bytes * steps * world / (ms_max / 1e3) / 1e9, 1),
+        "unit": "GB/s",
+        "h2d_bytes_per_step": int(hq.numel() * 2 + hcu.numel() * 4),
+        "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4),
+        "steps": steps,
+        "ms_per_step": round(ms_max / steps, 4),
+        "pipeline": "one step at a time on one stream; the KV cache stays resident",
     }
 
 
@@ -727,8 +895,13 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the sliding-window and block-sparse prefill measurements")
-    ap.add_argument("--only", choices=["both", "prefill", "decode"], default="both",
-                    help="run one half of the step (for profiling)")
+    ap.add_argument("--only", choices=["both", "prefill", "decode", "configs"], default="both",
+                    help="run one half of the step, or only the table of other prefill "
+                         "workloads (for profiling)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the table of other prefill workloads")
+    ap.add_argument("--config", default=None,
+                    help="time only this workload of the table (a name from synthetic.py)")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="sequences of the decode workload (first B of the seeded lengths)")
     ap.add_argument("--prefill-heads", type=int, default=64,
