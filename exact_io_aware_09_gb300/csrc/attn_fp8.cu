@@ -5,14 +5,15 @@
 // with random sign flips) before quantisation, so that (Q M)(K M)^T = Q K^T while outlier
 // channels spread over all channels, and the operands are quantised to E4M3 with per-block
 // scaling factors.  This file writes, from the 16-bit inputs:
-//   Q8, K8   E4M3 codes of the rotated rows, [planes, N, d], one scale per 128-row tile
-//            (amax of the rotated tile / 448);
+//   Q8, K8   E4M3 codes of the rotated rows, [planes, N, d], one scale per 128-row tile;
 //   V^T8     E4M3 codes of V (not rotated), transposed to [planes, d, nkvp] (the K-major B
 //            operand of the 8-bit P V product), one scale per plane;
-// then runs the FP8 variant of the prefill kernel on them.  The rotation runs in fp32 with the
-// fast Walsh-Hadamard butterflies in a fixed order (stage h = 1, 2, ..., d/2: (a, b) ->
-// (a + b, a - b)), then one multiply by the fp32 value of 1/sqrt(d); the codes are
-// E4M3(x / scale) with an IEEE division, nearest even, saturating.
+// then runs the FP8 variant of the prefill kernel on them.  A block's scale is a power of two:
+// the smallest 2^e with amax <= 448 * 2^e (448 is E4M3's largest value), so that the codes
+// E4M3(x * 2^-e) (nearest even, saturating) come from an exact multiply instead of a division.
+// The rotation runs in fp32 with the fast Walsh-Hadamard butterflies in a fixed order (stage
+// h = 1, 2, ..., d/2: (a, b) -> (a + b, a - b)), then one multiply by the fp32 value of
+// 1/sqrt(d).
 #include <type_traits>
 
 #include "internal.h"
@@ -79,8 +80,20 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
-__device__ __forceinline__ float scale_of(float amax) {
-  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+// Exponent e of a block's scale 2^e: the smallest with amax <= 448 * 2^e, at least -126 so
+// that 2^e and 2^-e are normal fp32 values; 0 for an all-zero block.  With amax = (1 + M/2^23)
+// 2^(E-127), amax <= 1.75 * 2^(8+e) holds from e = E - 135 when the mantissa is at most 0.75
+// (1.75 = 448 / 2^8), from e = E - 134 otherwise.
+__device__ __forceinline__ int scale_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  const uint32_t b = __float_as_uint(amax);
+  const int E = static_cast<int>((b >> 23) & 0xffu);
+  const int e = ((b & 0x7fffffu) <= 0x600000u) ? E - 135 : E - 134;
+  return e < -126 ? -126 : e;
+}
+
+__device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
 }  // namespace
@@ -172,19 +185,16 @@ __global__ void __launch_bounds__(kRotThreads)
 #pragma unroll
   for (int c = 0; c < kH; ++c) amax = fmaxf(amax, fabsf(v[c]));
   // 3. tile amax, scale, codes (the block reduction's barriers also end every read of the stage)
-  const float scale = scale_of(block_max(amax, red));
-  if (threadIdx.x == 0) (is_q ? sq : sk)[b] = scale;
+  const int e = scale_exp(block_max(amax, red));
+  if (threadIdx.x == 0) (is_q ? sq : sk)[b] = exp2i(e);
+  const float inv = exp2i(-e);
 #pragma unroll
   for (int c = 0; c < kH; c += 16) {
     uint4 w;
-    w.x = pack4_e4m3(__fdiv_rn(v[c + 0], scale), __fdiv_rn(v[c + 1], scale),
-                     __fdiv_rn(v[c + 2], scale), __fdiv_rn(v[c + 3], scale));
-    w.y = pack4_e4m3(__fdiv_rn(v[c + 4], scale), __fdiv_rn(v[c + 5], scale),
-                     __fdiv_rn(v[c + 6], scale), __fdiv_rn(v[c + 7], scale));
-    w.z = pack4_e4m3(__fdiv_rn(v[c + 8], scale), __fdiv_rn(v[c + 9], scale),
-                     __fdiv_rn(v[c + 10], scale), __fdiv_rn(v[c + 11], scale));
-    w.w = pack4_e4m3(__fdiv_rn(v[c + 12], scale), __fdiv_rn(v[c + 13], scale),
-                     __fdiv_rn(v[c + 14], scale), __fdiv_rn(v[c + 15], scale));
+    w.x = pack4_e4m3(v[c + 0] * inv, v[c + 1] * inv, v[c + 2] * inv, v[c + 3] * inv);
+    w.y = pack4_e4m3(v[c + 4] * inv, v[c + 5] * inv, v[c + 6] * inv, v[c + 7] * inv);
+    w.z = pack4_e4m3(v[c + 8] * inv, v[c + 9] * inv, v[c + 10] * inv, v[c + 11] * inv);
+    w.w = pack4_e4m3(v[c + 12] * inv, v[c + 13] * inv, v[c + 14] * inv, v[c + 15] * inv);
     *reinterpret_cast<uint4*>(stage + my_row * kCodePitch + half * kH + c) = w;
   }
   __syncthreads();
@@ -231,8 +241,9 @@ __global__ void __launch_bounds__(kPrepThreads)
   constexpr int kPitch = kT + 4;  // bytes per channel row in shared memory
   __shared__ __align__(16) uint8_t tile[D * kPitch];
   const int plane = blockIdx.x / n_tiles, kt = blockIdx.x % n_tiles;
-  const float scale = scale_of(__uint_as_float(amax_bits[plane]));
-  if (kt == 0 && threadIdx.x == 0) scales[plane] = scale;
+  const int e = scale_exp(__uint_as_float(amax_bits[plane]));
+  if (kt == 0 && threadIdx.x == 0) scales[plane] = exp2i(e);
+  const float inv = exp2i(-e);
   const uint16_t* src = x + static_cast<size_t>(plane) * N * D;
   constexpr int kChunks = D / 8;                 // 8-channel chunks of a row
   constexpr int kUnits = (kT / 4) * kChunks;     // (key quad, chunk) pairs
@@ -245,10 +256,8 @@ __global__ void __launch_bounds__(kPrepThreads)
       if (key < N) {
         float v[8];
         load8<BF16>(src + static_cast<size_t>(key) * D + chunk * 8, v);
-        w[r][0] = pack4_e4m3(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale),
-                             __fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale));
-        w[r][1] = pack4_e4m3(__fdiv_rn(v[4], scale), __fdiv_rn(v[5], scale),
-                             __fdiv_rn(v[6], scale), __fdiv_rn(v[7], scale));
+        w[r][0] = pack4_e4m3(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+        w[r][1] = pack4_e4m3(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
       } else {
         w[r][0] = w[r][1] = 0u;
       }

@@ -135,8 +135,10 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
  *   workspace  device, >= attn_fwd_fp8_workspace_bytes(...) bytes, caller-owned; receives the
  *              E4M3 operands and their scales (layout: attn_fwd_fp8_workspace_offsets)
  * Q and K rows are rotated (fp32, fast Walsh-Hadamard butterflies) and quantised with one scale
- * per 128-row tile (amax / 448); V is quantised with one scale per (batch, key/value head) and
- * stored transposed; P enters the P V product as E4M3.  O is written in `dtype`, L in fp32 as
+ * per 128-row tile; V is quantised with one scale per (batch, key/value head) and stored
+ * transposed.  Each scale is a power of two, the smallest 2^e with amax <= 448 * 2^e (448: the
+ * largest E4M3 value; 1 for an all-zero block), and the codes are E4M3(x * 2^-e), nearest even.
+ * P enters the P V product as E4M3.  O is written in `dtype`, L in fp32 as
  * attn_fwd.  Returns ATTN_OK or a negative attn_status_t.
  */
 size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int N_q, int N_kv, int d);

@@ -15,8 +15,9 @@ Steps, each written out here:
      value of 1/sqrt(d).  The rotation decides integer codes below, so it is evaluated in the
      precision and order the kernel uses (fp32).
   2. Block quantisation: one scale per 128-row tile of a (batch, head) plane for Q and K
-     (amax of the tile / 448, the largest E4M3 value) and one per plane for V (not rotated);
-     code = E4M3(x / scale) rounded to nearest even, saturating at +-448.
+     and one per plane for V (not rotated).  A scale is a power of two, the smallest 2^e with
+     amax <= 448 * 2^e (448 is the largest E4M3 value; e >= -126; 1 for an all-zero block);
+     code = E4M3(x * 2^-e) rounded to nearest even, saturating at +-448.
   3. Attention in fp64 of the dequantised operands (code value * scale): the same definition as
      the prefill oracle, on these inputs.
 Readings where the pages are silent (block shape, V's scale, the P conversion of the kernel)
@@ -91,10 +92,20 @@ def rotate_f32(x, signs):
     return y * np.float32(1.0 / np.sqrt(np.float32(d)))
 
 
+def pow2_scale(amax):
+    """Block scales for the amax values (float32 array): the smallest power of two 2^e with
+    amax <= 448 * 2^e, e >= -126; 1 where amax is 0.  With amax = f 2^k, f in [0.5, 1), and
+    448 = 0.875 * 2^9: e = k - 9 when f <= 0.875, else k - 8."""
+    a = np.asarray(amax, dtype=np.float64)
+    f, k = np.frexp(a)
+    e = np.maximum(np.where(f <= 0.875, k - 9, k - 8), -126)
+    return np.where(a > 0, np.ldexp(1.0, e), 1.0).astype(np.float32)
+
+
 def quantize_tiles(x, rows_per_tile=128):
     """x float32 [planes, N, d] -> (codes uint8 [planes, N, d], scales float32 [planes, tiles]).
-    One scale per 128-row tile: amax / 448 (1 for an all-zero tile); codes = E4M3(x / scale),
-    the division in fp32."""
+    One power-of-two scale per 128-row tile (pow2_scale of the tile's amax); codes =
+    E4M3(x / scale), an exact power-of-two scaling."""
     x = np.asarray(x, dtype=np.float32)
     P, N, d = x.shape
     nt = -(-N // rows_per_tile)
@@ -102,20 +113,19 @@ def quantize_tiles(x, rows_per_tile=128):
     scales = np.ones((P, nt), dtype=np.float32)
     for t in range(nt):
         blk = x[:, t * rows_per_tile:(t + 1) * rows_per_tile]
-        amax = np.abs(blk).reshape(P, -1).max(axis=1)
-        sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        sc = pow2_scale(np.abs(blk).reshape(P, -1).max(axis=1))
         scales[:, t] = sc
         codes[:, t * rows_per_tile:(t + 1) * rows_per_tile] = e4m3_encode(
-            (blk / sc[:, None, None]).astype(np.float32))
+            blk.astype(np.float64) / sc[:, None, None].astype(np.float64))
     return codes, scales
 
 
 def quantize_planes(x):
-    """x float32 [planes, N, d] -> (codes, scales [planes]): one scale per plane."""
+    """x float32 [planes, N, d] -> (codes, scales [planes]): one power-of-two scale per plane."""
     x = np.asarray(x, dtype=np.float32)
     amax = np.abs(x).reshape(x.shape[0], -1).max(axis=1) if x.size else np.zeros(x.shape[0])
-    sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    return e4m3_encode((x / sc[:, None, None]).astype(np.float32)), sc
+    sc = pow2_scale(amax)
+    return e4m3_encode(x.astype(np.float64) / sc[:, None, None].astype(np.float64)), sc
 
 
 def prepare(q, k, v, signs):
@@ -177,8 +187,8 @@ def fp8_attention(q, k, v, signs, causal, scale):
 def fp8_attention_per_tensor(q, k, v, causal, scale):
     """The baseline FP8 attention the pages compare incoherent processing against ("FlashAttention
     Explained", section "FP8 Attention and Incoherent Processing"): no rotation and one scale per
-    tensor (amax of all of Q, of all of K, of all of V, over 448), then exact attention of the
-    dequantised operands.  q, k, v float32.  Returns (o, lse)."""
+    tensor (all of Q, all of K, all of V; the same power-of-two rule as the blocks), then exact
+    attention of the dequantised operands.  q, k, v float32.  Returns (o, lse)."""
     B, Hq, Nq, d = q.shape
     _, Hkv, Nkv, _ = k.shape
     deq = []

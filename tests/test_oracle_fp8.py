@@ -72,8 +72,26 @@ def test_quantisation_error_is_at_most_half_a_step():
         a = np.abs(blk).astype(np.float64)
         step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(a, 1e-30))), -6) - 3)
         assert np.all(np.abs(deq - blk) <= step / 2 + 1e-12)
-    # the tile holding the outlier reaches the top of the E4M3 range exactly
-    assert np.abs(fp8.e4m3_decode(codes[0, :128])).max() == 448.0
+    # the tile holding the outlier, 60 = 240 * 2^-2, reaches the upper half of the E4M3 range
+    assert scales[0, 0] == 0.25 and np.abs(fp8.e4m3_decode(codes[0, :128])).max() == 240.0
+
+
+def test_block_scale_is_the_smallest_power_of_two_that_fits():
+    """pow2_scale: 2^e with amax <= 448 * 2^e < 2 * amax, checked against the definition at the
+    boundaries (448 itself, the next float up, powers of two, tiny and huge values)."""
+    f32 = np.float32
+    vals = np.array([448.0, np.nextafter(f32(448.0), f32(1e9)), 224.0, 1.0, 3.0, 60.0, 1e-30,
+                     2.0 ** -120, 3e38, 1.0 / 3.0], dtype=np.float32)
+    sc = fp8.pow2_scale(vals).astype(np.float64)
+    for a, s_ in zip(vals.astype(np.float64), sc):
+        m, e = np.frexp(s_)
+        assert m == 0.5                              # a power of two
+        if e - 1 > -126:
+            assert a <= 448.0 * s_ < 2 * a + 1e-300  # and the smallest that fits
+        else:
+            assert a <= 448.0 * s_ and s_ == 2.0 ** -126
+    assert list(sc[:4]) == [1.0, 2.0, 0.5, 2.0 ** -8]
+    assert fp8.pow2_scale(np.float32(0.0)) == 1.0
 
 
 def test_f64_attention_matches_the_prefill_oracle():
@@ -102,9 +120,9 @@ def test_rotation_leaves_unquantised_scores_unchanged():
 
 def test_prepare_dequantises_to_the_rotated_inputs():
     """prepare + dequantized: each value is within half an E4M3 step (times its block's scale)
-    of the rotated Q / K and the unrotated V; the scales are amax / 448 of the right block (128
+    of the rotated Q / K and the unrotated V; the scales are those of the right block (128
     rows of one (batch, head) plane for Q and K, the whole plane for V); planes are (batch,
-    head) in that order."""
+    head) in that order.  Every scale is the smallest power of two 2^e with amax <= 448 * 2^e."""
     rng = np.random.default_rng(21)
     B, Hq, Hkv, Nq, Nkv, d = 2, 4, 2, 200, 150, 64
     q = rng.standard_normal((B, Hq, Nq, d)).astype(np.float32)
@@ -126,7 +144,8 @@ def test_prepare_dequantises_to_the_rotated_inputs():
                 for t in range(-(-n_ // rows)):
                     blk = ref[b, h, t * rows:(t + 1) * rows]
                     s = sc[b * h_ + h, t]
-                    assert abs(s - np.abs(blk).max() / 448.0) <= 1e-6 * s
+                    amax = float(np.abs(blk).max())
+                    assert amax <= 448.0 * s * (1 + 1e-6) and 448.0 * s < 2 * amax * (1 + 1e-6)
                     err = np.abs(got[b, h, t * rows:(t + 1) * rows] - blk)
                     # half a step of E4M3 (2^-4 relative, 2^-10 absolute below 2^-6) plus the
                     # fp32 rotation's rounding
@@ -135,7 +154,7 @@ def test_prepare_dequantises_to_the_rotated_inputs():
     for b in range(B):
         for h in range(Hkv):
             s = prep["sv"][b * Hkv + h]
-            assert s == np.float32(np.abs(v[b, h]).max() / np.float32(448.0))
+            assert s == fp8.pow2_scale(np.abs(v[b, h]).max())
             err = np.abs(vd[b, h] - v[b, h])
             assert np.all(err <= s * np.maximum(np.abs(v[b, h]) / s * 2.0 ** -4, 2.0 ** -10))
     # the outlier's tile: the rotation spreads 40 over 64 channels (5 each), about twice the
