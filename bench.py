@@ -98,7 +98,7 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None

@@ -775,14 +775,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             x[c] += __uint_as_float((((vis[c >> 5] >> (c & 31)) & 1u) - 1u) & 0xff800000u);
         }
-        // Row maximum of the tile: three-input max, eight independent chains.
-        float mx[8];
+        // Row maximum of the tile: three-input max, sixteen independent chains.
+        float mx[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(x[e], x[8 + e]);
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(x[e], x[16 + e]);
 #pragma unroll
-        for (int c = 16; c < kBlockN; c += 16)
+        for (int c = 32; c < kBlockN; c += 32)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mx[e] = max3f(mx[e], x[c + e], x[c + 8 + e]);
+          for (int e = 0; e < 16; ++e) mx[e] = max3f(mx[e], x[c + e], x[c + 16 + e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
         const float tile_max = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
                                      fmaxf(mx[6], mx[7]));
         // Running maximum after tile t - 1, from the other warpgroup (on the first tile of an
@@ -819,17 +821,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_own = m_j;
         }
         const float neg_mu = ((m_j == -INFINITY) ? 0.0f : -m_j) + (FP8 ? kPShift8 : 0);
-        // p = 2^(x * scale * log2(e) - m): one packed FMA per pair of scores, MUFU ex2, a packed
-        // add into four pair-accumulators for the row sum, and the 16-bit pack for P (FP8:
-        // 2^5 p, four E4M3 codes per word).
+        // p = 2^(x * scale * log2(e) - m): one packed FMA per pair of scores and MUFU ex2, all
+        // of them first (in place, so that consecutive ex2 depend on nothing but their own FMA),
+        // then a packed add into four pair-accumulators for the row sum and the 16-bit pack for
+        // P (FP8: 2^5 p, four E4M3 codes per word).
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 2) {
+          float a0, a1;
+          fma2(a0, a1, x[c], x[c + 1], tsc, tsc, neg_mu, neg_mu);
+          x[c] = ex2(a0);
+          x[c + 1] = ex2(a1);
+        }
         float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[2][32];
 #pragma unroll
         for (int c = 0; c < kBlockN; c += 4) {
-          float a0, a1, a2, a3;
-          fma2(a0, a1, x[c], x[c + 1], tsc, tsc, neg_mu, neg_mu);
-          fma2(a2, a3, x[c + 2], x[c + 3], tsc, tsc, neg_mu, neg_mu);
-          const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+          const float p0 = x[c], p1 = x[c + 1], p2 = x[c + 2], p3 = x[c + 3];
           const int k2 = ((c >> 1) & 3) * 2;
           add2(ps[k2], ps[k2 + 1], p0, p1);
           add2(ps[k2 + 2], ps[k2 + 3], p2, p3);

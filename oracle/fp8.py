@@ -102,6 +102,30 @@ def pow2_scale(amax):
     return np.where(a > 0, np.ldexp(1.0, e), 1.0).astype(np.float32)
 
 
+def hadamard_sylvester(d):
+    """The d x d Sylvester-Hadamard matrix (d a power of two): H_1 = [1],
+    H_2k = [[H_k, H_k], [H_k, -H_k]]."""
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def rotate_exact(x, signs):
+    """Rows of x -> H (s o x) / sqrt(d) as one fp64 matrix product with the explicit matrix:
+    independent of the butterfly order the fp32 rotation follows."""
+    d = np.asarray(x).shape[-1]
+    M = hadamard_sylvester(d) * np.asarray(signs, dtype=np.float64)[None, :] / np.sqrt(d)
+    return np.asarray(x, dtype=np.float64) @ M.T
+
+
+def e4m3_spacing(x):
+    """Spacing of the E4M3 values around |x| (2^-9 in the subnormal range)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -30)))
+    return np.exp2(np.maximum(e, -6) - 3)
+
+
 def quantize_tiles(x, rows_per_tile=128):
     """x float32 [planes, N, d] -> (codes uint8 [planes, N, d], scales float32 [planes, tiles]).
     One power-of-two scale per 128-row tile (pow2_scale of the tile's amax); codes =

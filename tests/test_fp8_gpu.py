@@ -153,6 +153,35 @@ def test_preparation_is_bit_exact(attn, shape):
     assert not got["vt8"][:, :, Nkv:].any(), "V^T padding keys must hold code 0"
 
 
+@pytest.mark.parametrize("shape", [s for s in PREP if s[-1]], ids=lambda s: "x".join(map(str, s)))
+def test_codes_are_within_a_step_of_the_exact_rotation(attn, shape):
+    """Independent of the butterfly order: the kernel's Q and K codes against the rows rotated
+    in fp64 by the explicit Sylvester-Hadamard matrix (oracle.fp8.rotate_exact) and divided by
+    the kernel's block scales. A correctly rounded code lies within half an E4M3 spacing of that
+    value; the fp32 rotation's rounding may tip one to its neighbour, never further. The scales
+    are the smallest powers of two above amax / 448 of the exact rotation."""
+    B, Hq, Hkv, Nq, Nkv, dt, _ = shape
+    d = 128
+    cfg = syn.PrefillConfig("fp8", B, Hq, Hkv, Nq, Nkv, d, dt, True, 900 + sum(shape[:5]))
+    q, k, v = cfg.host_inputs()
+    q = syn.with_outliers(q, dt, cfg.seed + 11)
+    signs = syn.random_signs(d, cfg.seed + 12)
+    _, _, ws = run_fp8(attn, q, k, v, dt, True, cfg.scale, signs, keep_workspace=True)
+    got = workspace_parts(ws, attn, B, Hq, Hkv, Nq, Nkv, d)
+    for x, codes, sc, N in ((q, got["q8"], got["sq"], Nq), (k, got["k8"], got["sk"], Nkv)):
+        exact = fp8.rotate_exact(as_f32(x, dt).reshape(-1, N, d), signs)
+        s_rows = np.repeat(sc.astype(np.float64), 128, axis=1)[:, :N, None]
+        y = exact / s_rows
+        deq = fp8.e4m3_decode(codes)
+        far = np.abs(deq - y) > fp8.e4m3_spacing(y)
+        assert not far.any(), f"{int(far.sum())} codes more than one step from the exact value"
+        assert (codes == fp8.e4m3_encode(y)).mean() > 0.99
+        for pl in range(exact.shape[0]):
+            for t in range(sc.shape[1]):
+                a = np.abs(exact[pl, t * 128:(t + 1) * 128]).max()
+                assert a <= 448.0 * sc[pl, t] * (1 + 1e-6) and 448.0 * sc[pl, t] < 2 * a * (1 + 1e-6)
+
+
 PARITY = [
     # (B, Hq, Hkv, N_q, N_kv, dtype, causal)
     (1, 1, 1, 128, 128, "bf16", False),

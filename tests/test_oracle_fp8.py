@@ -197,3 +197,23 @@ def test_per_tensor_baseline_lets_one_outlier_set_every_scale():
     o_blk, _, _ = fp8.fp8_attention(q, k, v, None, False, d ** -0.5)
     err = lambda o: float(np.sqrt(np.mean((o[0, 1] - exact[0, 1]) ** 2)))
     assert err(o_base) > 2 * err(o_blk), (err(o_base), err(o_blk))
+
+
+def test_fp32_rotation_codes_are_within_a_step_of_the_exact_rotation():
+    """The codes of the fp32 butterfly rotation (the order the kernel uses) against E4M3 of the
+    same rows rotated in fp64 by the explicit Sylvester-Hadamard matrix, with the same scales:
+    every code within one E4M3 spacing of the exact value and nearly all identical."""
+    rng = np.random.default_rng(41)
+    d = 128
+    x = rng.standard_normal((2, 300, d)).astype(np.float32)
+    x[0, 3, 9] = 50.0
+    signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    H = np.asarray(__import__("scipy.linalg", fromlist=["hadamard"]).hadamard(d), np.float64)
+    np.testing.assert_array_equal(fp8.hadamard_sylvester(d), H)
+    codes, scales = fp8.quantize_tiles(fp8.rotate_f32(x, signs))
+    exact = fp8.rotate_exact(x, signs)
+    sc = np.repeat(scales, 128, axis=1)[:, :300, None].astype(np.float64)
+    y = exact / sc
+    deq = fp8.e4m3_decode(codes)
+    assert np.all(np.abs(deq - y) <= fp8.e4m3_spacing(y))
+    assert (codes == fp8.e4m3_encode(y)).mean() > 0.99
