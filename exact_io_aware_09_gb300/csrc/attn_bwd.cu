@@ -257,6 +257,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The dQ kernel needs nothing this one writes: its blocks may take the SMs this grid's
+  // blocks leave, as soon as every block of this grid has started.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   // job: key tile kt of (batch, key/value head) bkv, numbered key tile major; the launch order
   // is the packed one of KvOrder when the launcher gives one
@@ -900,6 +903,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kBwdTmemCols);
   }
+  // This grid may have started while the dK/dV kernel was still running; no block of it
+  // finishes before that kernel has, so that whatever follows on the stream sees dK and dV
+  // complete.
+  if (threadIdx.x == 0) griddep_wait();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1071,7 +1078,18 @@ static int launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
   kkv<<<static_cast<unsigned>(kv_blocks), kKvThreads, LK::kBytes, stream>>>(tq64, tk, tv, tdo64, p,
                                                                             *order);
   if (cudaGetLastError() != cudaSuccess) return -5;
-  kq<<<static_cast<unsigned>(q_blocks), kQThreads, LQ::kBytes, stream>>>(tk, tv, tdo, p);
+  // dQ as a programmatic dependent of dK/dV: its blocks fill the SMs of dK/dV's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(q_blocks));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = LQ::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kq, tk, tv, tdo, p) != cudaSuccess) return -5;
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

@@ -370,6 +370,19 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 }
 
 // ------------------------------------------------------------------------------------------
+// programmatic dependent launch
+// ------------------------------------------------------------------------------------------
+// This block allows the stream's next kernel, when that was launched as a programmatic
+// dependent, to be scheduled once every block of this grid has said so or has exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one was launched to depend on have completed and their memory
+// operations are visible (returns at once in a kernel launched without such a dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------------
 // named barriers
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
