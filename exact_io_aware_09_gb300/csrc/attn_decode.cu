@@ -402,9 +402,18 @@ __global__ void __launch_bounds__(kDecThreads)
 // Merge the chunk states of one (sequence, query head) row:
 //   m = max_s m_s,  w_s = 2^(m_s - m) l_s,  l = sum_s w_s,  o = sum_s w_s o_s / l,
 //   L = ln 2 * (m + log2 l).
+// One warp finds m over the row's splits (its lanes striding over them) and the block writes
+// the weights w_s of up to kMergeChunk splits at a time to shared memory; then every thread sums
+// its channel over those splits with eight independent loads in flight, in split order.  A row
+// has up to max_seqlen / split splits (64 for 32k tokens at 512): walked one after the other,
+// each load would wait a full memory latency.
+constexpr int kMergeChunk = 256;
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(D)
     attn_decode_merge_kernel(const DecParams p, uint16_t* out, float* lse) {
+  __shared__ float w_s[kMergeChunk];
+  __shared__ float row_max;
   const int hq = blockIdx.x;
   const int b = blockIdx.y;
   const int col = threadIdx.x;
@@ -418,13 +427,43 @@ __global__ void __launch_bounds__(D)
     return;
   }
   const size_t part0 = row * p.max_splits;
-  float mm = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) mm = fmaxf(mm, p.ws_ml[(part0 + s) * 2]);
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + part0;  // (m, l) per split
+  if (threadIdx.x < 32) {
+    float m = -INFINITY;
+    for (int s = threadIdx.x; s < n_splits; s += 32) m = fmaxf(m, ml[s].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) row_max = m;
+  }
+  __syncthreads();
+  const float mm = row_max;
   float ll = 0.f, acc = 0.f;
-  for (int s = 0; s < n_splits; ++s) {
-    const float w = ex2(p.ws_ml[(part0 + s) * 2] - mm) * p.ws_ml[(part0 + s) * 2 + 1];
-    ll += w;
-    acc += w * p.ws_o[(part0 + s) * D + col];
+  for (int c0 = 0; c0 < n_splits; c0 += kMergeChunk) {
+    const int nc = min(kMergeChunk, n_splits - c0);
+    for (int s = threadIdx.x; s < nc; s += D) {
+      const float2 v = ml[c0 + s];
+      w_s[s] = ex2(v.x - mm) * v.y;
+    }
+    __syncthreads();
+    const float* o = p.ws_o + (part0 + c0) * D + col;
+    int s = 0;
+    for (; s + 8 <= nc; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = o[static_cast<size_t>(s + u) * D];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = w_s[s + u];
+        ll += w;
+        acc += w * v[u];
+      }
+    }
+    for (; s < nc; ++s) {
+      const float w = w_s[s];
+      ll += w;
+      acc += w * o[static_cast<size_t>(s) * D];
+    }
+    __syncthreads();  // every thread has read this chunk's weights
   }
   const float v = acc / ll;
   uint32_t pk = pack2<BF16>(v, 0.f);
