@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(kDecThreads)
   const int split = blockIdx.x;
   const int hk = blockIdx.y;
   const int b = blockIdx.z;
+  // the merge kernel may be scheduled once every block of this grid has started (it waits for
+  // this grid's completion before reading anything)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   int t_start, t_stop;
   if (!seq_bounds(p, b, t_start, t_stop)) {
     if (split == 0 && hk == 0 && threadIdx.x == 0) latch_status(p.status, kStatusBadLengths);
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kDecThreads)
 //   L = ln 2 * (m + log2 l).
 // One warp finds m over the row's splits (its lanes striding over them) and the block writes
 // the weights w_s of up to kMergeChunk splits at a time to shared memory; then every thread sums
-// its channel over those splits with eight independent loads in flight, in split order.  A row
+// its channel over those splits with sixteen independent loads in flight, in split order.  A row
 // has up to max_seqlen / split splits (64 for 32k tokens at 512): walked one after the other,
 // each load would wait a full memory latency.
 constexpr int kMergeChunk = 256;
@@ -414,6 +417,9 @@ __global__ void __launch_bounds__(D)
     attn_decode_merge_kernel(const DecParams p, uint16_t* out, float* lse) {
   __shared__ float w_s[kMergeChunk];
   __shared__ float row_max;
+  // launched as a programmatic dependent of the split kernel: its partial states are complete
+  // and visible once this returns
+  griddep_wait();
   const int hq = blockIdx.x;
   const int b = blockIdx.y;
   const int col = threadIdx.x;
@@ -447,12 +453,12 @@ __global__ void __launch_bounds__(D)
     __syncthreads();
     const float* o = p.ws_o + (part0 + c0) * D + col;
     int s = 0;
-    for (; s + 8 <= nc; s += 8) {
-      float v[8];
+    for (; s + 16 <= nc; s += 16) {
+      float v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = o[static_cast<size_t>(s + u) * D];
+      for (int u = 0; u < 16; ++u) v[u] = o[static_cast<size_t>(s + u) * D];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const float w = w_s[s + u];
         ll += w;
         acc += w * v[u];
@@ -533,8 +539,22 @@ static int launch_decode_variant(const DecodeArgs& a, cudaStream_t stream) {
     kern<<<grid, kDecThreads, L::kBytes, stream>>>(tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
   }
-  dim3 mgrid(a.Hq, a.B);
-  attn_decode_merge_kernel<D, BF16><<<mgrid, D, 0, stream>>>(p, static_cast<uint16_t*>(a.o), a.lse);
+  // The merge goes out as a programmatic dependent of the kernel before it (the split kernel,
+  // or whatever the stream ran last): its blocks are scheduled early and wait at their start
+  // (griddepcontrol.wait) until that grid has completed, which hides the launch gap.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hq, a.B);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<D, BF16>, p, static_cast<uint16_t*>(a.o),
+                         a.lse) != cudaSuccess)
+    return -5;
   return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
