@@ -156,6 +156,9 @@ __global__ void __launch_bounds__(kDecThreads)
       __syncwarp();
     }
     if (lane == 0) {
+      // The cache is streamed once: its lines go first out of L2, so that the partial states
+      // this grid writes are still there when the merge reads them.
+      const uint64_t stream_policy = l2_policy_evict_first();
       int issued = 0;
       for (int st = 0; st < n_stages; ++st) {
         const int s = st % kDecStages;
@@ -167,8 +170,8 @@ __global__ void __launch_bounds__(kDecThreads)
         const int tl = t0 + st * kDecTok;  // first token of the stage
         if (!p.block_table) {
           mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
-          tma_load_4d(kbuf, &tm_k, FULL(s), 0, tl, 0, hk);
-          tma_load_4d(vbuf, &tm_v, FULL(s), 0, tl, 0, hk);
+          tma_load_4d_hint(kbuf, &tm_k, FULL(s), 0, tl, 0, hk, stream_policy);
+          tma_load_4d_hint(vbuf, &tm_v, FULL(s), 0, tl, 0, hk, stream_policy);
         } else {
           // Pages of this stage that hold tokens of the sequence: one when a page spans the
           // whole stage (its rows tl .. tl + 63 lie in one page), else 64 / page_size pages
@@ -197,8 +200,8 @@ __global__ void __launch_bounds__(kDecThreads)
           for (int i = 0; i < kDecTok / 16; ++i) {
             if (phys[i] < 0) continue;
             const uint32_t box_off = static_cast<uint32_t>(i) * (D / 64) * rows * 128u;
-            tma_load_4d(kbuf + box_off, &tm_k, FULL(s), 0, phys[i], 0, hk);
-            tma_load_4d(vbuf + box_off, &tm_v, FULL(s), 0, phys[i], 0, hk);
+            tma_load_4d_hint(kbuf + box_off, &tm_k, FULL(s), 0, phys[i], 0, hk, stream_policy);
+            tma_load_4d_hint(vbuf + box_off, &tm_v, FULL(s), 0, phys[i], 0, hk, stream_policy);
           }
         }
         issued = st + 1;
