@@ -155,60 +155,73 @@ __global__ void __launch_bounds__(kDecThreads)
       }
       __syncwarp();
     }
-    if (lane == 0) {
-      // The cache is streamed once: its lines go first out of L2, so that the partial states
-      // this grid writes are still there when the merge reads them.
-      const uint64_t stream_policy = l2_policy_evict_first();
-      int issued = 0;
-      for (int st = 0; st < n_stages; ++st) {
-        const int s = st % kDecStages;
-        if (st >= kDecStages &&
-            !wait_bounded(EMPTY(s), ((st / kDecStages) - 1) & 1, abort_flag, p.status))
-          break;
-        const uint32_t kbuf = base + s * L::kStage;
-        const uint32_t vbuf = kbuf + L::kTensor;
-        const int tl = t0 + st * kDecTok;  // first token of the stage
-        if (!p.block_table) {
+    // The cache is streamed once: its lines go first out of L2, so that the partial states this
+    // grid writes are still there when the merge reads them.
+    const uint64_t stream_policy = l2_policy_evict_first();
+    if (!p.block_table) {
+      if (lane == 0) {
+        int issued = 0;
+        for (int st = 0; st < n_stages; ++st) {
+          const int s = st % kDecStages;
+          if (st >= kDecStages &&
+              !wait_bounded(EMPTY(s), ((st / kDecStages) - 1) & 1, abort_flag, p.status))
+            break;
+          const uint32_t kbuf = base + s * L::kStage;
+          const uint32_t vbuf = kbuf + L::kTensor;
+          const int tl = t0 + st * kDecTok;  // first token of the stage
           mbar_arrive_expect_tx(FULL(s), 2 * L::kTensor);
           tma_load_4d_hint(kbuf, &tm_k, FULL(s), 0, tl, 0, hk, stream_policy);
           tma_load_4d_hint(vbuf, &tm_v, FULL(s), 0, tl, 0, hk, stream_policy);
-        } else {
-          // Pages of this stage that hold tokens of the sequence: one when a page spans the
-          // whole stage (its rows tl .. tl + 63 lie in one page), else 64 / page_size pages
-          // loaded to consecutive row blocks of the stage.  Rows past the sequence end are
-          // masked by the compute warps.  A block-table entry outside the page pool is
-          // reported and its load skipped.
-          const int rows = min(p.page_size, kDecTok);
-          const int n_pg = kDecTok / rows;
-          const int first = t0 >> p.page_log2;
-          uint32_t bytes = 0;
-          int phys[kDecTok / 16];
-#pragma unroll
-          for (int i = 0; i < kDecTok / 16; ++i) {
-            phys[i] = -1;
-            const int t = tl + i * rows;
-            if (i < n_pg && t < t_stop) {
-              const int r0 = page_row[(t >> p.page_log2) - first];
-              if (r0 >= 0) {
-                phys[i] = r0 + (t & (p.page_size - 1));
-                bytes += 2u * (D / 64) * rows * 128u;  // both tensors, both channel halves
-              }
-            }
+          issued = st + 1;
+        }
+        for (int st = (issued > kDecStages ? issued - kDecStages : 0); st < issued; ++st)
+          wait_bounded(FULL(st % kDecStages), (st / kDecStages) & 1, nullptr, p.status,
+                       100000000ull);
+      }
+    } else {
+      // Pages of a stage that hold tokens of the sequence: one when a page spans the whole
+      // stage (its rows tl .. tl + 63 lie in one page), else 64 / page_size pages loaded to
+      // consecutive row blocks of the stage, each by its own lane (lane i: page i of the stage),
+      // so that the copies of small pages go out side by side.  Lane 0 waits for the ring slot
+      // and arms its barrier with the stage's bytes first.  Rows past the sequence end are
+      // masked by the compute warps; a block-table entry outside the page pool is reported and
+      // its load skipped.
+      const int rows = min(p.page_size, kDecTok);
+      const int n_pg = kDecTok / rows;
+      const int first = t0 >> p.page_log2;
+      const uint32_t page_bytes = 2u * (D / 64) * rows * 128u;  // K and V, both channel halves
+      int issued = 0;
+      for (int st = 0; st < n_stages; ++st) {
+        const int s = st % kDecStages;
+        bool ok = true;
+        if (lane == 0 && st >= kDecStages)
+          ok = wait_bounded(EMPTY(s), ((st / kDecStages) - 1) & 1, abort_flag, p.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const uint32_t kbuf = base + s * L::kStage;
+        const uint32_t vbuf = kbuf + L::kTensor;
+        const int tl = t0 + st * kDecTok;  // first token of the stage
+        int phys = -1;
+        if (lane < n_pg) {
+          const int t = tl + lane * rows;
+          if (t < t_stop) {
+            const int r0 = page_row[(t >> p.page_log2) - first];
+            if (r0 >= 0) phys = r0 + (t & (p.page_size - 1));
           }
-          mbar_arrive_expect_tx(FULL(s), bytes);
-#pragma unroll
-          for (int i = 0; i < kDecTok / 16; ++i) {
-            if (phys[i] < 0) continue;
-            const uint32_t box_off = static_cast<uint32_t>(i) * (D / 64) * rows * 128u;
-            tma_load_4d_hint(kbuf + box_off, &tm_k, FULL(s), 0, phys[i], 0, hk, stream_policy);
-            tma_load_4d_hint(vbuf + box_off, &tm_v, FULL(s), 0, phys[i], 0, hk, stream_policy);
-          }
+        }
+        const uint32_t n_loads = __popc(__ballot_sync(0xffffffffu, phys >= 0));
+        if (lane == 0) mbar_arrive_expect_tx(FULL(s), n_loads * page_bytes);
+        __syncwarp();
+        if (phys >= 0) {
+          const uint32_t box_off = static_cast<uint32_t>(lane) * (D / 64) * rows * 128u;
+          tma_load_4d_hint(kbuf + box_off, &tm_k, FULL(s), 0, phys, 0, hk, stream_policy);
+          tma_load_4d_hint(vbuf + box_off, &tm_v, FULL(s), 0, phys, 0, hk, stream_policy);
         }
         issued = st + 1;
       }
-      for (int st = (issued > kDecStages ? issued - kDecStages : 0); st < issued; ++st)
-        wait_bounded(FULL(st % kDecStages), (st / kDecStages) & 1, nullptr, p.status,
-                     100000000ull);
+      if (lane == 0)
+        for (int st = (issued > kDecStages ? issued - kDecStages : 0); st < issued; ++st)
+          wait_bounded(FULL(st % kDecStages), (st / kDecStages) & 1, nullptr, p.status,
+                       100000000ull);
     }
     return;  // the producer takes no part in the reduction below
   }
