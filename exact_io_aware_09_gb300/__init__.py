@@ -18,6 +18,7 @@ __all__ = [
     "attn_decode_splitkv", "attn_decode_workspace_bytes", "attn_decode_paged",
     "attn_decode_splitkv_static", "attn_decode_static_scratch_bytes",
     "attn_poll_status", "attn_status_string", "attn_fwd_kv_tiles", "attn_fwd_kv_span",
+    "attn_fwd_set_d64_kernel", "D64_AUTO", "D64_PAIR", "D64_SINGLE",
     "attn_bwd_kv_order", "attn_selftest_timeout",
     "attn_version", "library_path", "lib",
 ]
@@ -73,6 +74,8 @@ lib.attn_status_string.argtypes = [_I]
 lib.attn_status_string.restype = ctypes.c_char_p
 lib.attn_fwd_kv_tiles.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
 lib.attn_fwd_kv_tiles.restype = _I
+lib.attn_fwd_set_d64_kernel.argtypes = [_I]
+lib.attn_fwd_set_d64_kernel.restype = _I
 lib.attn_bwd_kv_order.argtypes = [_I] * 7 + [ctypes.POINTER(ctypes.c_uint16), _I, ctypes.POINTER(_I)]
 lib.attn_bwd_kv_order.restype = _I
 lib.attn_fwd_kv_span.argtypes = [_I, _I, _I, _I, _I, _I, _I] + [ctypes.POINTER(_I)] * 4
@@ -442,6 +445,18 @@ def attn_fwd_kv_tiles(q_tile: int, block_m: int, block_n: int, N_q: int, N_kv: i
     _check(lib.attn_fwd_kv_tiles(q_tile, block_m, block_n, N_q, N_kv, int(bool(causal)),
                                  ctypes.byref(n), ctypes.byref(fm)), "attn_fwd_kv_tiles")
     return n.value, fm.value
+
+
+D64_AUTO, D64_PAIR, D64_SINGLE = 0, 1, 2
+
+
+def attn_fwd_set_d64_kernel(mode: int) -> int:
+    """Choose the d = 64 prefill kernel for later calls (D64_AUTO, D64_PAIR: two query tiles per
+    work item, D64_SINGLE: one); returns the previous mode."""
+    r = int(lib.attn_fwd_set_d64_kernel(int(mode)))
+    if r < 0:
+        raise AttnError(r, "attn_fwd_set_d64_kernel")
+    return r
 
 
 def attn_bwd_kv_order(B: int, Hq: int, Hkv: int, N_q: int, N_kv: int, causal: bool, n_sm: int,

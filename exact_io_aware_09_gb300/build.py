@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_decode.cu", "attn_bwd.cu", "attn_fp8.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_decode.cu", "attn_bwd.cu",
+           "attn_fp8.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h")] + [
     os.path.join(ROOT, "include", "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

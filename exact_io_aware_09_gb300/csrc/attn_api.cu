@@ -419,6 +419,11 @@ const char* attn_status_string(int status) {
   }
 }
 
+int attn_fwd_set_d64_kernel(int mode) {
+  const int prev = attn::set_d64_kernel(mode);
+  return prev < 0 ? ATTN_ERR_INVALID_ARG : prev;
+}
+
 int attn_fwd_kv_tiles(int q_tile, int block_m, int block_n, int N_q, int N_kv, int causal,
                       int* n_tiles, int* first_masked) {
   if (q_tile < 0 || block_m <= 0 || block_n <= 0 || N_q < 0 || N_kv < 0 || !n_tiles ||

@@ -38,6 +38,7 @@
 // accumulator is rescaled only when a row maximum rises by more than 2^8 (the final division uses
 // the same stale maximum in l, so the result is unchanged: "FlashAttention Explained", section on
 // FlashAttention-4, conditional rescaling).
+#include <atomic>
 #include <cstdio>
 
 #include "internal.h"
@@ -1048,6 +1049,13 @@ extern "C" int attn_fwd_trace_copy(void* dst) {
 namespace attn {
 #endif
 
+static std::atomic<int> g_d64_mode{0};
+
+int set_d64_kernel(int mode) {
+  if (mode < 0 || mode > 2) return -1;
+  return g_d64_mode.exchange(mode);
+}
+
 int launch_attn_fwd_fp8_kernel(const FwdArgs& a, cudaStream_t stream) {
   if (a.d != 128) return -2;
   return a.bf16 ? launch_fwd_variant<128, true, 4, 4, true>(a, stream)
@@ -1066,9 +1074,23 @@ int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
       attn_empty_rows_kernel<false><<<blocks, 256, 0, stream>>>(static_cast<uint16_t*>(a.o), a.lse, rows, a.d);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
   }
-  if (a.d == 64)
+  if (a.d == 64) {
+    // Two query tiles per item when there are more query tiles than SMs (so that the pairs
+    // still cover every SM), else one.
+    const int mode = g_d64_mode.load();
+    bool pair = (mode == 1);
+    if (mode == 0) {
+      const uint64_t tiles = static_cast<uint64_t>(a.B) * a.Hq * ((a.N_q + kBlockM - 1) / kBlockM);
+      int dev = 0, n_sm = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -5;
+      pair = tiles > static_cast<uint64_t>(n_sm);
+    }
+    if (pair) return launch_attn_fwd_pair(a, stream);
     return a.bf16 ? launch_fwd_variant<64, true, 4, 4>(a, stream)
                   : launch_fwd_variant<64, false, 4, 4>(a, stream);
+  }
   if (a.d == 128)
     return a.bf16 ? launch_fwd_variant<128, true, 3, 2>(a, stream)
                   : launch_fwd_variant<128, false, 3, 2>(a, stream);

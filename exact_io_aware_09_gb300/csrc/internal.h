@@ -151,6 +151,10 @@ struct BwdArgs {
 
 // Launchers (return an attn_status_t value).
 int launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+// d = 64: two query tiles per work item (attn_fwd_pair.cu)
+int launch_attn_fwd_pair(const FwdArgs& a, cudaStream_t stream);
+// The d = 64 kernel choice: 0 automatic, 1 two query tiles per item, 2 one (attn_fwd.cu).
+int set_d64_kernel(int mode);
 int launch_attn_fwd_fp8_kernel(const FwdArgs& a, cudaStream_t stream);
 // FP8 forward: prepares the rotated, quantised operands in `workspace` (layout from
 // fp8_workspace_layout: Q8, K8, V^T8, Q scales, K scales, V scales, V amax) and runs the kernel.

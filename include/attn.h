@@ -357,6 +357,20 @@ int attn_bwd_kv_order(int B, int Hq, int Hkv, int N_q, int N_kv, int causal, int
                       uint16_t *job, int cap, int *n);
 
 /*
+ * attn_fwd_set_d64_kernel -- choose the prefill kernel for head dimension 64 (every later call
+ * of attn_fwd, attn_fwd_window and attn_fwd_block_sparse in this process, on every device):
+ *   ATTN_D64_AUTO (0, the default): two query tiles per work item, which share each K/V tile
+ *     ("FlashAttention Explained", section on FlashAttention-4: two query tiles per thread
+ *     block), when the call has more 128-row query tiles (B * Hq * ceil(N_q / 128)) than the
+ *     device has SMs; else one query tile per item, which spreads a small call over more SMs;
+ *   ATTN_D64_PAIR (1), ATTN_D64_SINGLE (2): always that kernel.
+ * Both compute the same operator within the same rounding.  Returns the previous mode, or
+ * ATTN_ERR_INVALID_ARG for any other value (the mode is then unchanged).  Thread-safe.
+ */
+enum { ATTN_D64_AUTO = 0, ATTN_D64_PAIR = 1, ATTN_D64_SINGLE = 2 };
+int attn_fwd_set_d64_kernel(int mode);
+
+/*
  * attn_selftest_timeout -- launch one tiny kernel that waits on a barrier nothing ever
  * arrives at, with a limit of `limit_us` microseconds (1 .. 1000000), then records
  * ATTN_ERR_TIMEOUT in the status word and returns.  Used to check, on a GPU, that a wait which

@@ -61,6 +61,14 @@ def test_status_strings(attn):
     assert attn.attn_status_string(123) == "unknown status"
 
 
+def test_d64_kernel_choice(attn):
+    assert attn.attn_fwd_set_d64_kernel(attn.D64_PAIR) == attn.D64_AUTO
+    assert attn.attn_fwd_set_d64_kernel(attn.D64_SINGLE) == attn.D64_PAIR
+    with pytest.raises(attn.AttnError):
+        attn.attn_fwd_set_d64_kernel(3)
+    assert attn.attn_fwd_set_d64_kernel(attn.D64_AUTO) == attn.D64_SINGLE  # 3 changed nothing
+
+
 def test_kv_tile_range_matches_page_exercise(golden, attn):
     g = golden("causal_tiles_ex4.json")
     # the page's tiles are 1-based with B_r = 128, B_c = 64

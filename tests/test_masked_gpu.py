@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import synthetic as syn
+from kernels import d64_kernel, d64_modes
 from parity import check_rows
 
 pytestmark = pytest.mark.gpu
@@ -56,32 +57,39 @@ WINDOW_CASES = [
     ((1, 2, 2, 100, 900, 128, "bf16"), 257),    # N_kv > N_q
     ((1, 2, 2, 1000, 1000, 128, "bf16"), 5000), # wider than the sequence: causal
     ((2, 96, 8, 520, 520, 128, "bf16"), 200),   # more items than SMs, GQA
+    ((2, 6, 2, 520, 520, 64, "f16"), 200),      # d = 64, 3 query heads per key/value head
 ]
 
 
 @pytest.mark.parametrize("shape,W", WINDOW_CASES, ids=lambda x: str(x))
 def test_window(attn, shape, W):
     cfg, (q, k, v) = _inputs(shape, 300 + W + sum(shape[:6]))
-    qt, kt, vt, o, lse = _gpu(cfg, q, k, v)
-    o, lse = attn.attn_fwd_window(qt, kt, vt, W, o=o, lse=lse, scale=cfg.scale)
-    assert attn.attn_poll_status() == 0
-    og, lg = _host(o, lse, cfg.d)
     orf, lrf = oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q,
                                      cfg.N_kv, cfg.d, True, cfg.scale, window=W)
-    check_rows(og, lg, orf, lrf, f"window {W} {shape}", dtype=cfg.dtype)
+    for mode in d64_modes(cfg.d):
+        qt, kt, vt, o, lse = _gpu(cfg, q, k, v)
+        with d64_kernel(attn, mode):
+            o, lse = attn.attn_fwd_window(qt, kt, vt, W, o=o, lse=lse, scale=cfg.scale)
+        assert attn.attn_poll_status() == 0
+        og, lg = _host(o, lse, cfg.d)
+        check_rows(og, lg, orf, lrf, f"window {W} {shape}, d = 64 kernel {mode}",
+                   dtype=cfg.dtype)
 
 
-def test_window_matches_causal_when_wide(attn):
+@pytest.mark.parametrize("d", [128, 64])
+def test_window_matches_causal_when_wide(attn, d):
     """W >= N_kv: the same result as attn_fwd's causal mask, bit for bit."""
     import torch
 
-    cfg, (q, k, v) = _inputs((1, 4, 2, 600, 600, 128, "bf16"), 77)
-    qt, kt, vt, o1, l1 = _gpu(cfg, q, k, v)
-    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
-    attn.attn_fwd(qt, kt, vt, o=o1, lse=l1, causal=True, scale=cfg.scale)
-    attn.attn_fwd_window(qt, kt, vt, 600, o=o2, lse=l2, scale=cfg.scale)
-    assert attn.attn_poll_status() == 0
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    cfg, (q, k, v) = _inputs((1, 4, 2, 600, 600, d, "bf16"), 77)
+    for mode in d64_modes(d):
+        qt, kt, vt, o1, l1 = _gpu(cfg, q, k, v)
+        o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+        with d64_kernel(attn, mode):
+            attn.attn_fwd(qt, kt, vt, o=o1, lse=l1, causal=True, scale=cfg.scale)
+            attn.attn_fwd_window(qt, kt, vt, 600, o=o2, lse=l2, scale=cfg.scale)
+        assert attn.attn_poll_status() == 0
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_window_pages_example_full_size(attn):
@@ -119,31 +127,37 @@ def test_block_sparse(attn, shape, causal, density):
     mask[0, :] = 0          # a query tile with no block at all
     if nkt > 1:
         mask[-1, :] = 1     # and one with every block
-    qt, kt, vt, o, lse = _gpu(cfg, q, k, v)
     mt = torch.from_numpy(mask).cuda()
-    o, lse = attn.attn_fwd_block_sparse(qt, kt, vt, mt, causal=causal, o=o, lse=lse,
-                                        scale=cfg.scale)
-    assert attn.attn_poll_status() == 0
-    og, lg = _host(o, lse, cfg.d)
     orf, lrf = oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q,
                                      cfg.N_kv, cfg.d, causal, cfg.scale, block_mask=mask,
                                      block=128)
-    check_rows(og, lg, orf, lrf, f"block-sparse {shape} causal={causal}",
-               dtype=cfg.dtype)
+    for mode in d64_modes(cfg.d):
+        qt, kt, vt, o, lse = _gpu(cfg, q, k, v)
+        with d64_kernel(attn, mode):
+            o, lse = attn.attn_fwd_block_sparse(qt, kt, vt, mt, causal=causal, o=o, lse=lse,
+                                                scale=cfg.scale)
+        assert attn.attn_poll_status() == 0
+        og, lg = _host(o, lse, cfg.d)
+        check_rows(og, lg, orf, lrf, f"block-sparse {shape} causal={causal}, d = 64 kernel {mode}",
+                   dtype=cfg.dtype)
 
 
-def test_block_sparse_all_ones_is_dense(attn):
+@pytest.mark.parametrize("d", [128, 64])
+def test_block_sparse_all_ones_is_dense(attn, d):
     import torch
 
-    cfg, (q, k, v) = _inputs((1, 4, 2, 600, 700, 128, "bf16"), 88)
+    cfg, (q, k, v) = _inputs((1, 4, 2, 600, 700, d, "bf16"), 88)
     qt, kt, vt, o1, l1 = _gpu(cfg, q, k, v)
     o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
     ones = torch.ones((5, 6), dtype=torch.uint8, device="cuda")
-    for causal in (False, True):
-        attn.attn_fwd(qt, kt, vt, o=o1, lse=l1, causal=causal, scale=cfg.scale)
-        attn.attn_fwd_block_sparse(qt, kt, vt, ones, causal=causal, o=o2, lse=l2, scale=cfg.scale)
-        assert attn.attn_poll_status() == 0
-        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for mode in d64_modes(d):
+        for causal in (False, True):
+            with d64_kernel(attn, mode):
+                attn.attn_fwd(qt, kt, vt, o=o1, lse=l1, causal=causal, scale=cfg.scale)
+                attn.attn_fwd_block_sparse(qt, kt, vt, ones, causal=causal, o=o2, lse=l2,
+                                           scale=cfg.scale)
+            assert attn.attn_poll_status() == 0
+            assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_masked_argument_errors(attn):

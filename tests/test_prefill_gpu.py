@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import synthetic as syn
+from kernels import d64_kernel, d64_modes
 from parity import check_rows
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +54,9 @@ SMALL = [
     (1, 2, 2, 400, 100, 64, "f16", True),      # N_kv < N_q: top rows see no key
     (1, 3, 1, 517, 517, 128, "bf16", True),    # 3 query heads per key/value head
     (1, 8, 1, 384, 384, 64, "f16", True),      # 8 query heads per key/value head
+    (1, 6, 2, 300, 300, 64, "bf16", True),     # d = 64, 3 query heads per key/value head: one
+                                               # head of each group without a partner
+    (1, 2, 2, 300, 300, 64, "f16", False),     # d = 64, odd number of query tiles
     (2, 2, 2, 640, 640, 128, "f16", False),
     (1, 2, 2, 1000, 1000, 128, "bf16", True),
     (1, 1, 1, 255, 4000, 64, "bf16", False),   # long key side, short query side
@@ -66,6 +70,7 @@ MANY_ITEMS = [
     (2, 80, 16, 300, 100, 64, "bf16", True),   # a third of the items see no key
     (1, 96, 8, 700, 700, 128, "f16", True),    # 1 to 6 K/V tiles per item
     (4, 64, 64, 130, 130, 64, "bf16", False),  # two tiles each, every other item 2 rows
+    (1, 48, 48, 840, 840, 64, "f16", True),    # d = 64, seven query tiles a head (odd tail)
     (2, 200, 50, 128, 64, 128, "bf16", False), # one tile each
     (1, 160, 160, 257, 1000, 128, "bf16", True),
 ]
@@ -76,9 +81,11 @@ def test_small_shapes(attn, shape):
     B, Hq, Hkv, Nq, Nkv, d, dt, causal = shape
     cfg = syn.PrefillConfig("small", B, Hq, Hkv, Nq, Nkv, d, dt, causal, 100 + sum(shape[:6]))
     q, k, v = cfg.host_inputs()
-    og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, f"shape {shape}", dtype=dt)
+    for mode in d64_modes(d):
+        with d64_kernel(attn, mode):
+            og, lg = run_gpu(attn, cfg, q, k, v)
+        check_rows(og, lg, orf, lrf, f"shape {shape}, d = 64 kernel {mode}", dtype=dt)
 
 
 @pytest.mark.parametrize("shape", MANY_ITEMS, ids=lambda s: "x".join(map(str, s)))
@@ -86,9 +93,11 @@ def test_many_items(attn, shape):
     B, Hq, Hkv, Nq, Nkv, d, dt, causal = shape
     cfg = syn.PrefillConfig("items", B, Hq, Hkv, Nq, Nkv, d, dt, causal, 200 + sum(shape[:6]))
     q, k, v = cfg.host_inputs()
-    og, lg = run_gpu(attn, cfg, q, k, v)
     orf, lrf = oracle_rows(cfg, q, k, v)
-    check_rows(og, lg, orf, lrf, f"shape {shape}", dtype=dt)
+    for mode in d64_modes(d):
+        with d64_kernel(attn, mode):
+            og, lg = run_gpu(attn, cfg, q, k, v)
+        check_rows(og, lg, orf, lrf, f"shape {shape}, d = 64 kernel {mode}", dtype=dt)
 
 
 def test_output_16_byte_aligned(attn):
