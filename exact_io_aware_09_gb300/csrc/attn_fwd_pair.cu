@@ -19,8 +19,10 @@
 //
 // Roles (384 threads): warps 0-3 and 4-7 the softmax warpgroups of query tiles 0 and 1
 // (thread = query row); warp 8 the scheduler and the TMA producer of Q (double-buffered by item
-// parity) and the K ring; warp 11 the V ring; warp 9 issues S_w = Q_w K^T (and owns tensor
-// memory), warp 10 O_w += P_w V.  The online-softmax step, the conditional rescale (only when
+// parity) and of the K and V rings; warp 9 issues S_w = Q_w K^T for both tiles (and owns tensor
+// memory); warps 10 and 11 issue O_0 += P_0 V and O_1 += P_1 V, one each, so that neither tile's
+// P V queues behind the other's (a thread pushing eight MMAs through the pipe's short queue
+// is busy for hundreds of cycles).  The online-softmax step, the conditional rescale (only when
 // the row maximum rises by more than 2^8) and the epilogue O = a / l, L = m + ln l are those of
 // the d = 128 kernel ("FlashAttention and GPU Data Movement", section 3.1).
 #include <atomic>
@@ -37,7 +39,7 @@ constexpr int kTm = 128;  // query rows of a tile
 constexpr int kTn = 128;  // keys of a key tile
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kVProducerWarp = 11;
+constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp0 = 10, kPvWarp1 = 11;
 constexpr uint32_t kItemReaders = 3 + 8;  // lane 0 of warps 9, 10, 11 and of each softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRegsSoftmax = 184, kRegsIssue = 136;
@@ -46,6 +48,7 @@ constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // + 128 w, + 64 w, + 6
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTile = kTm * kD * 2;   // bytes of a Q, K or V tile (one swizzled sub-tile)
 constexpr int KS = 4, VS = 4;              // K and V ring slots
+static_assert(KS == VS, "one producer loop fills both rings slot by slot");
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 struct PairParams {
@@ -74,7 +77,7 @@ enum PairBar : uint32_t {
   kBarItemFull = 14,  // [2] work-item ring slot written
   kBarItemEmpty = 16, // [2] ... and read by every role
   kBarClc = 18,       // cluster-launch-control answer landed
-  kBarDrain = 19,     // both issuers' MMAs finished (two commits)
+  kBarDrain = 19,     // the three issuers' MMAs finished (three commits)
   kNumFixedBars = 20
 };
 
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(BAR_V(s), 1);
-      mbar_init(BAR_VE(s), 1);
+      mbar_init(BAR_VE(s), 2);  // both P V issuers
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(FBAR(kBarQFull + b), 1);
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(FBAR(kBarItemEmpty + b), kItemReaders);
     }
     mbar_init(FBAR(kBarClc), 1);
-    mbar_init(FBAR(kBarDrain), 2);
+    mbar_init(FBAR(kBarDrain), 3);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -257,15 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kProducerWarp) {
     setmaxnreg_dec<kRegsIssue>();
     if (warp == kProducerWarp) {
-      // ------------------------------------------------------------- scheduler + Q/K producer
+      // ------------------------------------------------------------- scheduler + producer
       // Publishes the block's work items (its own first, then those of pending blocks it
-      // cancels) and loads, per item, the K tiles of its sequence, with the item's Q tiles
-      // after its first K tile (Q buffer by item parity, refilled once the score MMAs of the
-      // item two back finished).  The next item is asked for with the item's last K load; as
-      // soon as the answer is in, its Q tiles are pulled into L2.
+      // cancels) and loads, per item, the K and V tiles of its sequence, with the item's Q
+      // tiles after its first K tile (Q buffer by item parity, refilled once the score MMAs of
+      // the item two back finished).  The next item is asked for with the item's last K load;
+      // as soon as the answer is in, its Q tiles are pulled into L2.
       if (lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
         int id = static_cast<int>(blockIdx.x);
         int next_id = -1;
         bool clc_live = true, clc_pending = false;
@@ -318,6 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(BAR_K(s), kTile);
             tma_load_3d(sK + s * kTile, &tm_k, BAR_K(s), 0, j * kTn, it.kv_plane);
+            // V slot s (the rings have the same depth) once both P V of its previous tile finished
+            if (T >= VS && !wait_bounded(BAR_VE(s), ((T / VS) - 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(BAR_V(s), kTile);
+            tma_load_3d(sV + s * kTile, &tm_v, BAR_V(s), 0, j * kTn, it.kv_plane);
             ++T;
             if (first) {
               first = false;
@@ -349,54 +360,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           id = next_id;
         }
         // every asynchronous write into this block's shared memory lands before it may exit
-        for (int t = (T > KS ? T - KS : 0); t < T; ++t)
+        for (int t = (T > KS ? T - KS : 0); t < T; ++t) {
           wait_bounded(BAR_K(t % KS), (t / KS) & 1, nullptr, p.status, kDrainLimitNs);
+          wait_bounded(BAR_V(t % VS), (t / VS) & 1, nullptr, p.status, kDrainLimitNs);
+        }
         for (int q = (kq > 2 ? kq - 2 : 0); q < kq; ++q)
           wait_bounded(FBAR(kBarQFull + (q & 1)), (q >> 1) & 1, nullptr, p.status, kDrainLimitNs);
         if (clc_pending)
           wait_bounded(FBAR(kBarClc), clc_uses & 1, nullptr, p.status, kDrainLimitNs);
       }
       __syncwarp();
-    } else if (warp == kVProducerWarp) {
-      // ------------------------------------------------------------- V producer
-      if (lane == 0) {
-        prefetch_tmap(&tm_v);
-        int T = 0;
-        bool ok = true;
-        for (int k = 0; ok; ++k) {
-          int id;
-          if (!take_item(k, id)) break;
-          if (id < 0) break;
-          const PairItem it = decode_pair(id, p);
-          for (int j = it.u0; j < it.u1; ++j) {
-            if (!pair_sees(it, j)) continue;
-            const int s = T % VS;
-            if (T >= VS && !wait_bounded(BAR_VE(s), ((T / VS) - 1) & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(BAR_V(s), kTile);
-            tma_load_3d(sV + s * kTile, &tm_v, BAR_V(s), 0, j * kTn, it.kv_plane);
-            ++T;
-          }
-        }
-        for (int t = (T > VS ? T - VS : 0); t < T; ++t)
-          wait_bounded(BAR_V(t % VS), (t / VS) & 1, nullptr, p.status, kDrainLimitNs);
-      }
-      __syncwarp();
-    } else if (warp == kQkWarp || warp == kPvWarp) {
+    } else {
       // ------------------------------------------------------------- tcgen05 issuers
       // Warp 9: for each key tile of an item, S_w = Q_w K^T for the tiles w that see it, each
-      // once warpgroup w has read its previous S.  Warp 10: O_w (+)= P_w V for the same, each
-      // once P_w is stored; the first of an item overwrites O_w, after the previous item's
-      // epilogue has read it out.
+      // once warpgroup w has read its previous S.  Warp 10 + w: O_w (+)= P_w V for the key
+      // tiles query tile w sees, each once P_w is stored; the first of an item overwrites O_w,
+      // after the previous item's epilogue has read it out.  Each P V issuer arrives on every
+      // V slot's release once per key tile of the sequence, after seeing that slot's load (so
+      // that its arrival never counts toward the slot's previous use).
       if (lane == 0) {
         const bool qk_issuer = (warp == kQkWarp);
+        static_assert(kPvWarp1 == kPvWarp0 + 1, "P V issuers of query tiles 0 and 1");
+        const int pw = qk_issuer ? 0 : warp - kPvWarp0;  // the P V issuer's query tile
         constexpr uint32_t idesc_qk = make_idesc_f16(BF16, kTm, kTn, false);
         constexpr uint32_t idesc_pv = make_idesc_f16(BF16, kTm, kD, true);
         int T = 0, kq = 0;
-        int used[2] = {0, 0};   // products issued per query tile w
-        int items[2] = {0, 0};  // items in which query tile w had a key tile (P V issuer)
+        int used[2] = {0, 0};  // score products issued per query tile w (score issuer)
+        int pv_used = 0;       // P V products issued (P V issuer)
+        int pv_items = 0;      // items in which the issuer's query tile had a key tile
         bool ok = true;
         for (int k = 0; ok; ++k) {
           int id;
@@ -405,15 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const PairItem it = decode_pair(id, p);
           const int j_last = last_pair_tile(it);
           if (j_last < 0) continue;
+          const PairTile mine = pw ? it.t[1] : it.t[0];  // the P V issuer's query tile
           const int qb = kq & 1;
           if (qk_issuer && !wait_bounded(FBAR(kBarQFull + qb), (kq >> 1) & 1, abort_flag, p.status))
             break;
-          bool first[2] = {true, true};
+          bool pv_first = true;
           for (int j = it.u0; ok && j <= j_last; ++j) {
             if (!pair_sees(it, j)) continue;
-            bool waited = false;
             if (qk_issuer) {
               const int s = T % KS;
+              bool waited = false;
 #pragma unroll
               for (int w = 0; w < 2; ++w) {
                 if (!tile_sees(it.t[w], j)) continue;
@@ -444,23 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(BAR_KE(s));  // K slot free
             } else {
               const int s = T % VS;
-#pragma unroll
-              for (int w = 0; w < 2; ++w) {
-                if (!tile_sees(it.t[w], j)) continue;
-                if (!wait_bounded(FBAR(kBarPReady + w), used[w] & 1, abort_flag, p.status)) {
-                  ok = false;
-                  break;
-                }
-                if (!waited) {
-                  if (!wait_bounded(BAR_V(s), (T / VS) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                  }
-                  waited = true;
-                }
-                if (first[w] && items[w] >= 1 &&
-                    !wait_bounded(FBAR(kBarODrained + w), (items[w] - 1) & 1, abort_flag,
-                                  p.status)) {
+              if (!wait_bounded(BAR_V(s), (T / VS) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              if (!tile_sees(mine, j)) {
+                mbar_arrive(BAR_VE(s));  // nothing of this issuer reads the slot
+              } else {
+                if (!wait_bounded(FBAR(kBarPReady + pw), pv_used & 1, abort_flag, p.status) ||
+                    (pv_first && pv_items >= 1 &&
+                     !wait_bounded(FBAR(kBarODrained + pw), (pv_items - 1) & 1, abort_flag,
+                                   p.status))) {
                   ok = false;
                   break;
                 }
@@ -470,30 +456,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                   // V [keys, d], d contiguous: the MN-major B operand, 16 keys per MMA
                   const uint64_t bdesc =
                       make_sdesc_sw128(sV + s * kTile + kk * 16 * 128, 128 * 128, 1024);
-                  mma_ts(tmem + kColO + 64u * w, tmem + kColP + 64u * w + kk * 8, bdesc, idesc_pv,
-                         (!first[w] || kk > 0) ? 1u : 0u);
+                  mma_ts(tmem + kColO + 64u * pw, tmem + kColP + 64u * pw + kk * 8, bdesc,
+                         idesc_pv, (!pv_first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(FBAR(kBarPDone + w));
-                first[w] = false;
-                ++used[w];
+                mma_commit(FBAR(kBarPDone + pw));
+                mma_commit(BAR_VE(s));  // this issuer's reads of the V slot done
+                pv_first = false;
+                ++pv_used;
               }
-              if (!ok) break;
-              mma_commit(BAR_VE(s));  // V slot free
             }
             ++T;
           }
           if (!ok) break;
           if (qk_issuer) {
             mma_commit(FBAR(kBarQEmpty + qb));  // Q buffer free once these MMAs finished
-          } else {
-#pragma unroll
-            for (int w = 0; w < 2; ++w)
-              if (!first[w]) ++items[w];
+          } else if (!pv_first) {
+            ++pv_items;
           }
           ++kq;
         }
         // every MMA this thread issued completes before the block frees tensor memory
-        if (T > 0)
+        if (T > 0 && (qk_issuer || pv_used > 0))
           mma_commit(FBAR(kBarDrain));
         else
           mbar_arrive(FBAR(kBarDrain));
