@@ -14,6 +14,7 @@
 // The rotation runs in fp32 with the fast Walsh-Hadamard butterflies in a fixed order (stage
 // h = 1, 2, ..., d/2: (a, b) -> (a + b, a - b)), then one multiply by the fp32 value of
 // 1/sqrt(d).
+#include <atomic>
 #include <type_traits>
 
 #include "internal.h"
@@ -98,115 +99,165 @@ __device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127
 
 }  // namespace
 
-// One block per (plane, 128-row tile) of Q or of K (blocks [0, q_blocks) take Q): rotate
-// (optional), tile amax, quantise.  The tile passes through shared memory twice so that global
-// memory sees only coalesced 16-byte accesses: the 16-bit rows are loaded by consecutive threads,
-// then threads 2r and 2r + 1 take channels 0-63 and 64-127 of row r and run the butterfly stages
-// h = 1 .. 32 in registers, in the plain order; stage h = 64 pairs the two threads (the lower
-// keeps a + b, the upper computes a - b from the value it receives: the same fp32 operations).
-// Their E4M3 codes go back through shared memory and out as coalesced rows.
+// Rotation and quantisation of Q and K in one persistent launch: the (plane, 128-row tile)
+// tiles of Q and then those of K, numbered in that order, go round-robin over the blocks.  A
+// tile's two 64-channel halves come in by TMA (128-byte swizzle) into a four-deep ring, so
+// that the next three tiles load while this one is computed (one block per SM); threads 2r and 2r + 1 take channels
+// 0-63 and 64-127 of row r (reading their 16-byte chunks at the swizzled positions, free of
+// bank conflicts), apply the sign flips, run the butterfly stages h = 1 .. 32 in registers in
+// the plain order and stage h = 64 across the thread pair (the lower keeps a + b, the upper
+// computes a - b from the value it receives: the same fp32 operations), then x fp32(1/sqrt(d)),
+// the tile amax by a block reduction, the power-of-two scale and the codes by an exact multiply.
+// The codes go to a swizzled staging buffer (two, alternating by tile) and out by one TMA store.
 constexpr int kRotThreads = 2 * kT;
+constexpr int kRotStages = 4;
+constexpr uint32_t kRotHalf = kT * 64 * 2;        // one 64-channel half of a 16-bit tile
+constexpr uint32_t kRotIn = 2 * kRotHalf;          // a 16-bit tile (two halves)
+constexpr uint32_t kRotCodes = kT * 128;           // a tile of codes
+constexpr uint32_t kRotBars = kRotStages * kRotIn + 2 * kRotCodes;
+constexpr uint32_t kRotSmem = kRotBars + kRotStages * 8 + 2 * 8 * 4 + 1024;  // + alignment
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kRotThreads)
-    fp8_rotate_quantize_kernel(const uint16_t* xq, const uint16_t* xk, const int8_t* signs,
-                               float inv_sqrt_d, uint8_t* cq, uint8_t* ck, float* sq, float* sk,
-                               int Nq, int Nk, int nqt, int nkt, int q_blocks) {
+__global__ void __launch_bounds__(kRotThreads, 1)
+    fp8_rotate_quantize_kernel(const __grid_constant__ CUtensorMap tm_q,
+                               const __grid_constant__ CUtensorMap tm_k,
+                               const __grid_constant__ CUtensorMap tm_q8,
+                               const __grid_constant__ CUtensorMap tm_k8, const int8_t* signs,
+                               float inv_sqrt_d, float* sq, float* sk, int nqt, int nkt,
+                               int q_tiles, int n_tiles, int* status) {
   static_assert(D == 128, "two 64-channel halves per row");
-  constexpr int kH = D / 2;            // channels per thread
-  constexpr int kPitch = D * 2 + 16;   // bytes per staged 16-bit row
-  constexpr int kCodePitch = D + 16;   // bytes per staged code row
-  __shared__ __align__(16) uint8_t stage[kT * kPitch];
-  __shared__ float red[kRotThreads / 32];
-  const bool is_q = static_cast<int>(blockIdx.x) < q_blocks;
-  const int b = is_q ? blockIdx.x : blockIdx.x - q_blocks;
-  const int n_tiles = is_q ? nqt : nkt;
-  const int N = is_q ? Nq : Nk;
-  const uint16_t* x = is_q ? xq : xk;
-  uint8_t* codes = is_q ? cq : ck;
-  const int plane = b / n_tiles, tile = b % n_tiles;
-  const int rows = min(kT, N - tile * kT);
+  constexpr int kH = D / 2;  // channels per thread
+  extern __shared__ uint8_t rot_smem[];
+  const uint32_t raw = smem_u32(rot_smem);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = rot_smem + (base - raw);
+  const uint32_t bars = base + kRotBars;
+  float* red = reinterpret_cast<float*>(gbase + kRotBars + kRotStages * 8);  // [2][8]
   const int my_row = threadIdx.x >> 1, half = threadIdx.x & 1;
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (static_cast<size_t>(plane) * N +
-                                                               static_cast<size_t>(tile) * kT) * D);
-  // 1. coalesced load of the tile's rows (rows past the end read as zeros)
-  constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of a row
-#pragma unroll 4
-  for (int u = threadIdx.x; u < kT * kChunks; u += kRotThreads) {
-    const int row = u / kChunks, c = u % kChunks;
-    const uint4 w = row < rows ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D * 2 + c * 16)
-                               : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(stage + row * kPitch + c * 16) = w;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this block's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int my_tiles =
+      static_cast<int>(blockIdx.x) < n_tiles ? (n_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  auto load_tile = [&](int i) {  // this block's i-th tile into stage i % kRotStages
+    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const bool is_q = t < q_tiles;
+    const int b = is_q ? t : t - q_tiles;
+    const int nt = is_q ? nqt : nkt;
+    const uint32_t st = base + (i % kRotStages) * kRotIn;
+    const uint32_t bar = bars + 8u * (i % kRotStages);
+    mbar_arrive_expect_tx(bar, kRotIn);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      tma_load_3d(st + h * kRotHalf, is_q ? &tm_q : &tm_k, bar, h * 64, (b % nt) * kT, b / nt);
+  };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRotStages; ++s) mbar_init(bars + 8u * s, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;  // tiles whose loads thread 0 has issued
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    for (; issued < kRotStages && issued < my_tiles; ++issued) load_tile(issued);
   }
   // signs of this thread's 64 channels as two 32-bit masks (bit c set: channel negated)
   uint32_t neg[kH / 32] = {};
   if (signs) {
-    const int lane = threadIdx.x & 31;
     uint32_t all[D / 32];
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) all[q] = __ballot_sync(0xffffffffu, signs[q * 32 + lane] < 0);
 #pragma unroll
     for (int q = 0; q < kH / 32; ++q) neg[q] = half ? all[kH / 32 + q] : all[q];
   }
-  __syncthreads();
-  // 2. this thread's half row
-  float v[kH];
-#pragma unroll
-  for (int c = 0; c < kH / 8; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(stage + my_row * kPitch + half * kH * 2 + c * 16);
-    float f[8];
-    load8_words<BF16>(w, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[c * 8 + e] = f[e];
-  }
-  if (signs) {
-#pragma unroll
-    for (int c = 0; c < kH; ++c)
-      v[c] = __int_as_float(__float_as_int(v[c]) ^ (((neg[c >> 5] >> (c & 31)) & 1u) << 31));
-#pragma unroll
-    for (int h = 1; h < kH; h <<= 1)
-#pragma unroll
-      for (int j = 0; j < kH; ++j)
-        if ((j & h) == 0) {
-          const float a = v[j], c = v[j + h];
-          v[j] = a + c;
-          v[j + h] = a - c;
-        }
-    // h = 64: element j of the lower half with element j of the upper half
-#pragma unroll
-    for (int j = 0; j < kH; ++j) {
-      const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-      v[j] = half ? other - v[j] : v[j] + other;
+  bool ok = true;
+  int consumed = 0;  // tiles whose loads every thread has seen land
+  for (int i = 0; i < my_tiles; ++i) {
+    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const bool is_q = t < q_tiles;
+    const int b = is_q ? t : t - q_tiles;
+    const int nt = is_q ? nqt : nkt;
+    const int s = i % kRotStages;
+    const bool landed = wait_bounded(bars + 8u * s, (i / kRotStages) & 1, nullptr, status);
+    if (!__syncthreads_and(landed)) {
+      ok = false;
+      break;
     }
+    consumed = i + 1;
+    // 1. this thread's half row (16-byte chunk c of the row sits at chunk c ^ (row % 8))
+    const uint8_t* src = gbase + s * kRotIn + half * kRotHalf;
+    float v[kH];
 #pragma unroll
-    for (int c = 0; c < kH; ++c) v[c] = v[c] * inv_sqrt_d;
+    for (int c = 0; c < kH / 8; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src + sw128(my_row, c));
+      float f[8];
+      load8_words<BF16>(w, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[c * 8 + e] = f[e];
+    }
+    if (signs) {
+#pragma unroll
+      for (int c = 0; c < kH; ++c)
+        v[c] = __int_as_float(__float_as_int(v[c]) ^ (((neg[c >> 5] >> (c & 31)) & 1u) << 31));
+#pragma unroll
+      for (int h = 1; h < kH; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < kH; ++j)
+          if ((j & h) == 0) {
+            const float a = v[j], c = v[j + h];
+            v[j] = a + c;
+            v[j + h] = a - c;
+          }
+      // h = 64: element j of the lower half with element j of the upper half
+#pragma unroll
+      for (int j = 0; j < kH; ++j) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        v[j] = half ? other - v[j] : v[j] + other;
+      }
+#pragma unroll
+      for (int c = 0; c < kH; ++c) v[c] = v[c] * inv_sqrt_d;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kH; ++c) amax = fmaxf(amax, fabsf(v[c]));
+    // 2. tile amax (reduction slots alternate by tile); the block barrier also ends every read
+    // of stage s and, through thread 0's wait before it, the store that last read this tile's
+    // staging buffer
+    for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+    if (lane == 0) red[(i & 1) * 8 + warp] = amax;
+    if (threadIdx.x == 0) tma_store_wait_read1();
+    __syncthreads();
+    if (threadIdx.x == 0 && issued < my_tiles) load_tile(issued++);
+    float m = red[(i & 1) * 8];
+#pragma unroll
+    for (int w = 1; w < kRotThreads / 32; ++w) m = fmaxf(m, red[(i & 1) * 8 + w]);
+    const int e = scale_exp(m);
+    if (threadIdx.x == 0) (is_q ? sq : sk)[b] = exp2i(e);
+    const float inv = exp2i(-e);
+    // 3. codes: row r's 128 bytes, chunk c at chunk c ^ (r % 8) of staging buffer i % 2
+    uint8_t* codes = gbase + kRotStages * kRotIn + (i & 1) * kRotCodes;
+#pragma unroll
+    for (int c = 0; c < kH; c += 16) {
+      uint4 w;
+      w.x = pack4_e4m3(v[c + 0] * inv, v[c + 1] * inv, v[c + 2] * inv, v[c + 3] * inv);
+      w.y = pack4_e4m3(v[c + 4] * inv, v[c + 5] * inv, v[c + 6] * inv, v[c + 7] * inv);
+      w.z = pack4_e4m3(v[c + 8] * inv, v[c + 9] * inv, v[c + 10] * inv, v[c + 11] * inv);
+      w.w = pack4_e4m3(v[c + 12] * inv, v[c + 13] * inv, v[c + 14] * inv, v[c + 15] * inv);
+      *reinterpret_cast<uint4*>(codes + sw128(my_row, half * 4 + c / 16)) = w;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tma_store_3d(is_q ? &tm_q8 : &tm_k8, smem_u32(codes), 0, (b % nt) * kT, b / nt);
+      tma_store_commit();
+    }
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int c = 0; c < kH; ++c) amax = fmaxf(amax, fabsf(v[c]));
-  // 3. tile amax, scale, codes (the block reduction's barriers also end every read of the stage)
-  const int e = scale_exp(block_max(amax, red));
-  if (threadIdx.x == 0) (is_q ? sq : sk)[b] = exp2i(e);
-  const float inv = exp2i(-e);
-#pragma unroll
-  for (int c = 0; c < kH; c += 16) {
-    uint4 w;
-    w.x = pack4_e4m3(v[c + 0] * inv, v[c + 1] * inv, v[c + 2] * inv, v[c + 3] * inv);
-    w.y = pack4_e4m3(v[c + 4] * inv, v[c + 5] * inv, v[c + 6] * inv, v[c + 7] * inv);
-    w.z = pack4_e4m3(v[c + 8] * inv, v[c + 9] * inv, v[c + 10] * inv, v[c + 11] * inv);
-    w.w = pack4_e4m3(v[c + 12] * inv, v[c + 13] * inv, v[c + 14] * inv, v[c + 15] * inv);
-    *reinterpret_cast<uint4*>(stage + my_row * kCodePitch + half * kH + c) = w;
-  }
-  __syncthreads();
-  // 4. coalesced store of the code rows
-  uint8_t* dst = codes + (static_cast<size_t>(plane) * N + static_cast<size_t>(tile) * kT) * D;
-  constexpr int kCodeChunks = D / 16;
-#pragma unroll 4
-  for (int u = threadIdx.x; u < kT * kCodeChunks; u += kRotThreads) {
-    const int row = u / kCodeChunks, c = u % kCodeChunks;
-    if (row < rows)
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * D + c * 16) =
-          *reinterpret_cast<const uint4*>(stage + row * kCodePitch + c * 16);
+  if (threadIdx.x == 0) {
+    tma_store_wait_all();  // every code tile written before the block exits
+    // loads issued but not consumed (after a time-out) land before the shared memory goes away
+    for (int j = consumed; j < issued; ++j)
+      wait_bounded(bars + 8u * (j % kRotStages), (j / kRotStages) & 1, nullptr, status,
+                   100000000ull);
   }
 }
 
@@ -325,11 +376,32 @@ int launch_attn_fwd_fp8(const FwdArgs& a, const int8_t* signs, void* workspace,
   auto run = [&](auto bf16_tag) -> int {
     constexpr bool BF = decltype(bf16_tag)::value;
     const uint16_t* v16 = static_cast<const uint16_t*>(a.v);
-    fp8_rotate_quantize_kernel<D, BF><<<pq * nqt + pk * nkt, kRotThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), signs, inv_sqrt_d,
-        static_cast<uint8_t*>(const_cast<void*>(f.q8)), static_cast<uint8_t*>(const_cast<void*>(f.k8)),
-        const_cast<float*>(f.q_scale), const_cast<float*>(f.k_scale), a.N_q, a.N_kv, nqt, nkt,
-        pq * nqt);
+    CUtensorMap tq, tk, tq8, tk8;
+    const uint64_t rb = static_cast<uint64_t>(D) * 2;
+    if (!make_tmap_3d(&tq, a.q, BF, D, a.N_q, pq, rb, rb * a.N_q, 64, kT, 1) ||
+        !make_tmap_3d(&tk, a.k, BF, D, a.N_kv, pk, rb, rb * a.N_kv, 64, kT, 1) ||
+        !make_tmap_3d_u8(&tq8, f.q8, D, a.N_q, pq, D, static_cast<uint64_t>(D) * a.N_q, D, kT, 1) ||
+        !make_tmap_3d_u8(&tk8, f.k8, D, a.N_kv, pk, D, static_cast<uint64_t>(D) * a.N_kv, D, kT, 1))
+      return -5;
+    int* status = device_status_ptr();
+    if (!status) return -5;
+    auto kern = fp8_rotate_quantize_kernel<D, BF>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem) !=
+        cudaSuccess)
+      return -5;
+    static std::atomic<int> n_sm{0};
+    if (n_sm.load() == 0) {
+      int dev = 0, v = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return -5;
+      n_sm.store(v);
+    }
+    const int tiles = pq * nqt + pk * nkt;
+    const int grid = tiles < n_sm.load() ? tiles : n_sm.load();  // one block per SM
+    kern<<<grid, kRotThreads, kRotSmem, stream>>>(
+        tq, tk, tq8, tk8, signs, inv_sqrt_d, const_cast<float*>(f.q_scale),
+        const_cast<float*>(f.k_scale), nqt, nkt, pq * nqt, tiles, status);
     fp8_plane_amax_kernel<D, BF><<<pk * nkt, kPrepThreads, 0, stream>>>(v16, amax, a.N_kv, nkt);
     fp8_v_transpose_kernel<D, BF><<<pk * nkt, kPrepThreads, 0, stream>>>(
         v16, amax, const_cast<float*>(f.v_scale), static_cast<uint8_t*>(const_cast<void*>(f.vt8)),
