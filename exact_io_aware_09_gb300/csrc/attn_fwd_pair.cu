@@ -315,18 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool first = true;
           for (int j = it.u0; j_last >= 0 && j <= j_last; ++j) {
             if (!pair_sees(it, j)) continue;
+            // slot s of both rings (they have the same depth): K once the score products of its
+            // previous tile finished, V once both P V products of its previous tile did; both
+            // waits come before either load, so that a wait that runs out leaves no copy that
+            // the drain below would miss
             const int s = T % KS;
-            if (T >= KS && !wait_bounded(BAR_KE(s), ((T / KS) - 1) & 1, abort_flag, p.status)) {
+            if (T >= KS && (!wait_bounded(BAR_KE(s), ((T / KS) - 1) & 1, abort_flag, p.status) ||
+                            !wait_bounded(BAR_VE(s), ((T / VS) - 1) & 1, abort_flag, p.status))) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(BAR_K(s), kTile);
             tma_load_3d(sK + s * kTile, &tm_k, BAR_K(s), 0, j * kTn, it.kv_plane);
-            // V slot s (the rings have the same depth) once both P V of its previous tile finished
-            if (T >= VS && !wait_bounded(BAR_VE(s), ((T / VS) - 1) & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
             mbar_arrive_expect_tx(BAR_V(s), kTile);
             tma_load_3d(sV + s * kTile, &tm_v, BAR_V(s), 0, j * kTn, it.kv_plane);
             ++T;
