@@ -19,7 +19,7 @@
  * evaluated one query row at a time: the row of S is materialised, then the row of P, then
  * the row of O.  Nothing is blocked, fused or reordered beyond that.
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *  - the scale is applied to the exact fp64 dot product (never pre-multiplied into Q);
  *  - causal masking is bottom-right aligned: key j is visible to query i iff
  *    j <= i + (N_kv - N_q); for N_q == N_kv this is the pages' "col <= row";

@@ -20,8 +20,8 @@ Steps, each written out here:
      code = E4M3(x * 2^-e) rounded to nearest even, saturating at +-448.
   3. Attention in fp64 of the dequantised operands (code value * scale): the same definition as
      the prefill oracle, on these inputs.
-Readings where the pages are silent (block shape, V's scale, the P conversion of the kernel)
-are listed in the design notes.
+Where the pages are silent the readings above are taken: the 128-row block shape, one scale per
+plane for V, and power-of-two scales.
 """
 import numpy as np
 
