@@ -130,6 +130,8 @@ PREP = [
     (2, 4, 2, 200, 333, "f16", True),     # ragged tiles on both sides
     (1, 3, 1, 517, 300, "bf16", False),   # no rotation: plain block scaling
     (1, 2, 1, 1, 1000, "bf16", True),     # a one-row query tile
+    (2, 32, 4, 2000, 1024, "bf16", True),  # 1,088 tiles: each block of the persistent preparation
+                                           # walks about seven, around its four-stage ring
 ]
 
 
