@@ -227,19 +227,6 @@ def visible_keys_blocks(N_q, N_kv, mask, causal, bs=128):
     return out
 
 
-def variant_pattern(N_q, N_kv, seed=11):
-    """Block pattern of the block-sparse measurement: the causal blocks, each kept with
-    probability 1/2, plus the diagonal and the first key block of every query tile."""
-    nq, nk = -(-N_q // 128), -(-N_kv // 128)
-    rng = np.random.default_rng(seed)
-    m = (rng.random((nq, nk)) < 0.5).astype(np.uint8)
-    for r in range(nq):
-        m[r, r + 1:] = 0
-        m[r, min(r, nk - 1)] = 1
-        m[r, 0] = 1
-    return m
-
-
 def time_oracle_prefill(cfg, q, k, v, budget_s=12.0, rows_per_batch=1024, seed=0):
     """The oracle's throughput on random rows of the workload, in batches of rows_per_batch rows
     per call (large enough that its fixed cost per call, about 75 ms, stays a small part)."""
@@ -565,7 +552,9 @@ def measure_variants(args, attn, pcfg, q, k, v, o, lse, stream, peaks, peak_src)
     import torch
 
     W = 1024
-    pattern = variant_pattern(pcfg.N_q, pcfg.N_kv)
+    import synthetic as syn
+
+    pattern = syn.causal_block_pattern(pcfg.N_q, pcfg.N_kv)
     mask = torch.from_numpy(pattern).to(q.device)
     per_head = {
         "window": visible_keys_window(pcfg.N_q, pcfg.N_kv, W).sum(),

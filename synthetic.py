@@ -231,6 +231,20 @@ PREFILL_CONFIGS = [CONFIG1, CONFIG2, CONFIG3A, CONFIG3B, CONFIG3SA, CONFIG3SB, C
 # ----------------------------------------------------------------------------------------
 # paged KV cache layout (input generation only: where each token of a packed cache goes)
 # ----------------------------------------------------------------------------------------
+def causal_block_pattern(N_q: int, N_kv: int, seed: int = 11, block: int = 128) -> np.ndarray:
+    """Block pattern of the block-sparse measurement, [ceil(N_q/block), ceil(N_kv/block)] uint8:
+    each block on or below the diagonal kept with probability 1/2, plus the diagonal block and
+    the first key block of every query tile (so that every row sees a key)."""
+    nq, nk = -(-N_q // block), -(-N_kv // block)
+    rng = np.random.default_rng(seed)
+    m = (rng.random((nq, nk)) < 0.5).astype(np.uint8)
+    for r in range(nq):
+        m[r, r + 1:] = 0
+        m[r, min(r, nk - 1)] = 1
+        m[r, 0] = 1
+    return m
+
+
 def paged_layout(lengths, page_size: int, seed: int, spare_pages: int = 3):
     """A shuffled page pool for sequences of the given lengths.
 

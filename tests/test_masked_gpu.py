@@ -5,8 +5,8 @@ section) with bottom-right alignment.  attn_fwd_block_sparse: a pattern of (quer
 blocks ("FlashAttention, annotated", section 3.3).  Shapes cover several tiles, ragged edges,
 windows inside one tile and across tiles, rows with no visible key, grouped-query heads, both
 head dimensions and both element types, and more work items than SMs; the sliding window of the
-pages' example (W = 1024) runs at the 8192-token GQA size, every row.  Tolerances are those of
-tests/parity.py.
+pages' example (W = 1024) and the measured block pattern run at the 8192-token GQA size, every
+row.  Tolerances are those of tests/parity.py.
 """
 import numpy as np
 import pytest
@@ -158,6 +158,27 @@ def test_block_sparse_all_ones_is_dense(attn, d):
                                            scale=cfg.scale)
             assert attn.attn_poll_status() == 0
             assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_block_sparse_measured_pattern_full_size(attn):
+    """The block pattern the bench line times (causal blocks kept with probability 1/2, the
+    diagonal and the first key block always) on the 70B-class GQA prefill (B=1, Hq=64, Hkv=8,
+    N=8192, d=128, bf16), in the bench's launch configuration: every row of every head against
+    the oracle."""
+    import torch
+
+    cfg = syn.CONFIG4
+    q, k, v = cfg.host_inputs()
+    pattern = syn.causal_block_pattern(cfg.N_q, cfg.N_kv)
+    qt, kt, vt, o, lse = _gpu(cfg, q, k, v)
+    o, lse = attn.attn_fwd_block_sparse(qt, kt, vt, torch.from_numpy(pattern).cuda(), causal=True,
+                                        o=o, lse=lse, scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    og, lg = _host(o, lse, cfg.d)
+    orf, lrf = oracle.attention_rows(q, k, v, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.N_q,
+                                     cfg.N_kv, cfg.d, True, cfg.scale, block_mask=pattern,
+                                     block=128)
+    check_rows(og, lg, orf, lrf, "measured block pattern at 8192", dtype=cfg.dtype)
 
 
 def test_masked_argument_errors(attn):
