@@ -105,7 +105,13 @@ def test_splitkv_workload_full(attn):
     cut = torch.from_numpy(cu).cuda()
     o, lse = attn.attn_decode_splitkv(qd, kd, vd, cut, int(lengths.max()), split_size=cfg.split,
                                       scale=cfg.scale)
+    # a second call gives the same bits (the merge adds the splits in a fixed order)
+    o2, lse2 = attn.attn_decode_splitkv(qd, kd, vd, cut, int(lengths.max()), split_size=cfg.split,
+                                        scale=cfg.scale)
     assert attn.attn_poll_status() == 0
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    del o2, lse2
     og = o.float().cpu().numpy().astype(np.float64).reshape(-1, cfg.d)
     lg = lse.cpu().numpy().astype(np.float64).reshape(-1)
     q, kc, vc = (syn.tensor_to_bits(t) for t in (qd, kd, vd))

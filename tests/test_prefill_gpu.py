@@ -100,6 +100,29 @@ def test_many_items(attn, shape):
         check_rows(og, lg, orf, lrf, f"shape {shape}, d = 64 kernel {mode}", dtype=dt)
 
 
+@pytest.mark.parametrize("shape", [(1, 96, 8, 700, 700, 128, "f16", True),
+                                   (2, 80, 16, 300, 100, 64, "bf16", True),
+                                   (4, 64, 64, 130, 130, 64, "bf16", False)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_repeated_calls_are_bit_identical(attn, shape):
+    """More work items than SMs, so that the blocks take over one another's items in an order
+    that changes from launch to launch: O and L must not depend on it (no atomics, a fixed
+    order of the sums within an item)."""
+    import torch
+
+    B, Hq, Hkv, Nq, Nkv, d, dt, causal = shape
+    cfg = syn.PrefillConfig("det", B, Hq, Hkv, Nq, Nkv, d, dt, causal, 300 + sum(shape[:6]))
+    q, k, v = cfg.device_inputs("cuda")
+    for mode in d64_modes(d):
+        with d64_kernel(attn, mode):
+            first = attn.attn_fwd(q, k, v, causal=causal, scale=cfg.scale)
+            for _ in range(3):
+                o, lse = attn.attn_fwd(q, k, v, causal=causal, scale=cfg.scale)
+                assert torch.equal(o.view(torch.int16), first[0].view(torch.int16)), mode
+                assert torch.equal(lse.view(torch.int32), first[1].view(torch.int32)), mode
+        assert attn.attn_poll_status() == 0
+
+
 def test_output_16_byte_aligned(attn):
     """O only 16-byte aligned (the API's minimum for every pointer)."""
     import torch
