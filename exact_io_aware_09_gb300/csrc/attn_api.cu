@@ -286,6 +286,9 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_si
   return decode_workspace_bytes(B, Hq, max_seqlen_k, split_size, d);
 }
 
+// The decode kernels index sequences by a grid's second or third dimension (at most 65,535).
+constexpr int kMaxDecodeBatch = 65535;
+
 int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* cu_seqlens_k, int kv_capacity, int max_seqlen_k, void* o,
                         float* lse, int B, int Hq, int Hkv, int d, int split_size, float scale,
@@ -298,6 +301,7 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B > kMaxDecodeBatch) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!q || !o || !lse || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
   if (max_seqlen_k > 0 && kv_capacity > 0 && (!k_cache || !v_cache)) return ATTN_ERR_INVALID_ARG;
@@ -329,6 +333,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
   if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B > kMaxDecodeBatch) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(num_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_pages_per_seq) * page_size < max_seqlen_k)
     return ATTN_ERR_INVALID_ARG;
@@ -366,6 +371,7 @@ int attn_decode_splitkv_static(const void* q, const void* k_cache, const void* v
   if (split_size < 64 || split_size > 8192 || split_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B > kMaxDecodeBatch) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!q || !o || !lse || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
   if (max_seqlen_k > 0 && kv_capacity > 0 && (!k_cache || !v_cache)) return ATTN_ERR_INVALID_ARG;

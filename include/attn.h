@@ -228,7 +228,9 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_seqlen_k, int split_si
  *                split_size, d) bytes, 16-byte aligned; its contents need no initialisation
  *   Query head h reads key/value head h / (Hq / Hkv); Hq / Hkv must be <= 16.
  *
- * Supported: d in {64, 128}; dtype F16 or BF16.  Returns ATTN_OK or a negative attn_status_t.
+ * Supported: d in {64, 128}; dtype F16 or BF16; B <= 65535 (the kernels index sequences by a
+ * grid dimension of that size; a larger batch returns ATTN_ERR_UNSUPPORTED before any launch:
+ * split it into several calls).  Returns ATTN_OK or a negative attn_status_t.
  * Calls that share a workspace must not overlap on the device.
  */
 int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
@@ -286,7 +288,8 @@ int attn_decode_splitkv_static(const void *q, const void *k_cache, const void *v
  *   num_pages     pages in the pool; page_size a power of two from 16 to 65536
  *   max_seqlen_k  upper bound of seqlens_k (<= max_pages_per_seq * page_size), sizes the grid
  *   o, lse, B, Hq, Hkv, d, split_size, scale, dtype, workspace, workspace_bytes, stream
- *                 as attn_decode_splitkv (the workspace size is attn_decode_workspace_bytes)
+ *                 as attn_decode_splitkv (the workspace size is attn_decode_workspace_bytes;
+ *                 B <= 65535)
  * The result equals attn_decode_splitkv on the gathered packed cache.  A length above
  * max_seqlen_k or a block-table entry outside [0, num_pages) is reported as
  * ATTN_ERR_BAD_LENGTHS by attn_poll_status (that sequence's output is then undefined).

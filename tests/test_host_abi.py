@@ -176,6 +176,13 @@ def test_bad_arguments_are_refused_before_launch(attn):
     assert dec(ws_bytes=16) == -4
     assert dec(ws=nul) == -4
     assert dec(cu=ctypes.c_void_p((1 << 20) + 2)) == -3
+    # more sequences than a grid dimension holds: refused before any launch
+    assert L.attn_decode_splitkv(fake, fake, fake, fake, 1024, 1024, fake, fake, 65536, 64, 8, 128,
+                                 512, s, 1, fake, 1 << 40, nul) == -2
+    assert L.attn_decode_splitkv_static(fake, fake, fake, fake, 1024, 1024, fake, fake, 65536, 64,
+                                        8, 128, 512, s, 1, nul) == -2
+    assert L.attn_decode_paged(fake, fake, fake, fake, fake, 64, 16, 64, 1024, fake, fake, 65536,
+                               64, 8, 128, 512, s, 1, fake, 1 << 40, nul) == -2
     if no_device:
         assert dec() == -7
     def fp8(d=128, ws_bytes=1 << 30, ws=fake, signs=nul, B=1, nkv=300):
