@@ -196,6 +196,37 @@ def test_long_workload_full(attn, cfg):
     check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)
 
 
+def test_more_than_2_31_elements_sampled(attn):
+    """Q and O of 2.29e9 elements (B=1, Hq=128, Hkv=8, N=140,000 with a ragged last tile, d=128,
+    bf16, causal), so that element offsets pass 2^31 in the last heads: sampled rows of the
+    first, a middle and the last query head (first and last rows, the ragged tail and random
+    rows) against the oracle, which gets those heads' Q, K and V copied back."""
+    import torch
+
+    cfg = syn.PrefillConfig("big", 1, 128, 8, 140000, 140000, 128, "bf16", True, 6001)
+    assert cfg.B * cfg.Hq * cfg.N_q * cfg.d > 2 ** 31
+    q, k, v = cfg.device_inputs("cuda")
+    o, lse = attn.attn_fwd(q, k, v, causal=True, scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    rng = np.random.default_rng(6002)
+    G = cfg.Hq // cfg.Hkv
+    for h in (0, 61, cfg.Hq - 1):
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, cfg.N_q - 129, cfg.N_q - 1],
+                                         np.arange(cfg.N_q - 96, cfg.N_q, 13),
+                                         rng.integers(0, cfg.N_q, 40)])).astype(np.int64)
+        qh = syn.tensor_to_bits(q[0, h].contiguous())
+        kh = syn.tensor_to_bits(k[0, h // G].contiguous())
+        vh = syn.tensor_to_bits(v[0, h // G].contiguous())
+        orf, lrf = oracle.attention_rows(qh, kh, vh, cfg.dtype, 1, 1, 1, cfg.N_q, cfg.N_kv,
+                                         cfg.d, True, cfg.scale, rows)
+        idx = torch.from_numpy(rows).cuda()
+        og = o[0, h].index_select(0, idx).float().cpu().numpy().astype(np.float64)
+        lg = lse[0, h].index_select(0, idx).cpu().numpy().astype(np.float64)
+        check_rows(og, lg, orf, lrf, f"2^31+ elements, head {h}", dtype=cfg.dtype)
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+
 def test_gqa_long_context_full(attn):
     """The 70B-class GQA causal prefill (B=1, Hq=64, Hkv=8, N=8192, d=128, bf16): every row of
     every head against the oracle."""
