@@ -1,7 +1,8 @@
 """GPU parity of the split-KV decode (attn_decode_splitkv through the C ABI) against the fp64
 oracle: ragged lengths around the 64-token stage and the split boundaries, empty sequences,
 1 to 16 query heads per key/value head, split sizes, garbage (NaN) in cache rows no sequence
-owns, a length beyond the promised maximum, and the full 64-sequence workload."""
+owns, a length beyond the promised maximum, the full 64-sequence workload, and a cache of more
+than 2^31 elements."""
 import numpy as np
 import pytest
 
@@ -118,3 +119,33 @@ def test_splitkv_workload_full(attn):
     del kd, vd
     orf, lrf = oracle.decode_rows(q, kc, vc, cu, cfg.dtype, cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.scale)
     check_rows(og, lg, orf, lrf, cfg.name, dtype=cfg.dtype)
+
+
+def test_cache_past_2_31_elements(attn):
+    """A packed cache of 2.25e9 elements per K and V (16 sequences of about 140,000 tokens,
+    Hkv=8, d=128, bf16), so that the last sequences' element offsets pass 2^31: the last two
+    sequences against the oracle, which gets their query rows and cache slices copied back."""
+    import torch
+
+    lengths = tuple([140000] * 14 + [139999, 150001])
+    cfg = syn.DecodeConfig("bigcache", 16, 64, 8, 128, "bf16", 7001, lengths_override=lengths)
+    lens = cfg.lengths()
+    cu = syn.cu_seqlens(lens)
+    assert int(cu[-2]) * cfg.Hkv * cfg.d > 2 ** 31
+    qd, kd, vd = cfg.device_inputs("cuda")
+    cut = torch.from_numpy(cu).cuda()
+    o, lse = attn.attn_decode_splitkv(qd, kd, vd, cut, int(lens.max()), split_size=cfg.split,
+                                      scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    b0 = cfg.B - 2
+    t0, t1 = int(cu[b0]), int(cu[cfg.B])
+    q = syn.tensor_to_bits(qd[b0:])
+    kc = syn.tensor_to_bits(kd[t0:t1])
+    vc = syn.tensor_to_bits(vd[t0:t1])
+    cu2 = (cu[b0:] - cu[b0]).astype(cu.dtype)
+    orf, lrf = oracle.decode_rows(q, kc, vc, cu2, cfg.dtype, 2, cfg.Hq, cfg.Hkv, cfg.d, cfg.scale)
+    og = o[b0:].float().cpu().numpy().astype(np.float64).reshape(-1, cfg.d)
+    lg = lse[b0:].cpu().numpy().astype(np.float64).reshape(-1)
+    check_rows(og, lg, orf, lrf, "cache past 2^31 elements", dtype=cfg.dtype)
+    del qd, kd, vd, o, lse
+    torch.cuda.empty_cache()
