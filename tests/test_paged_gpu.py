@@ -75,6 +75,45 @@ def test_paged_full_workload_equals_packed(attn):
         del kp, vp
 
 
+def test_paged_pool_past_2_31_elements_equals_packed(attn):
+    """A pool of 2.25e9 elements per K and V (16 sequences of 140,000 to 150,000 tokens, Hkv=8,
+    d=128, bf16): the packed cache itself read as consecutive 16-token pages, in reverse page
+    order per sequence so that the table is not the identity.  The same bits as the packed
+    decode, whose offsets past 2^31 are checked against the oracle in the decode tests."""
+    import torch
+
+    lengths = np.array([140000] * 14 + [140000, 150000], dtype=np.int64)
+    cfg = syn.DecodeConfig("bigpool", 16, 64, 8, 128, "bf16", 7101,
+                           lengths_override=tuple(int(x) for x in lengths))
+    cu = syn.cu_seqlens(lengths)
+    assert int(cu[-1]) * cfg.Hkv * cfg.d > 2 ** 31
+    q, kc, vc = cfg.device_inputs("cuda")
+    max_len = int(lengths.max())
+    o_ref, l_ref = attn.attn_decode_splitkv(q, kc, vc, torch.from_numpy(cu).cuda(), max_len,
+                                            scale=cfg.scale)
+    page = 16
+    n_pages = int(cu[-1]) // page
+    max_pages = max_len // page
+    table = np.zeros((cfg.B, max_pages), dtype=np.int32)
+    # store sequence b's pages in reverse: its token t sits in pool page p0 + n - 1 - t // 16
+    perm = np.empty(int(cu[-1]) // page, dtype=np.int64)
+    for b in range(cfg.B):
+        p0, n = int(cu[b]) // page, int(lengths[b]) // page
+        table[b, :n] = p0 + n - 1 - np.arange(n)
+        perm[p0:p0 + n] = p0 + np.arange(n)[::-1]
+    idx = torch.from_numpy(perm).cuda()
+    kp = kc.view(n_pages, page, cfg.Hkv, cfg.d).index_select(0, idx)
+    vp = vc.view(n_pages, page, cfg.Hkv, cfg.d).index_select(0, idx)
+    del kc, vc
+    seq = torch.from_numpy(lengths.astype(np.int32)).cuda()
+    o, l = attn.attn_decode_paged(q, kp, vp, torch.from_numpy(table).cuda(), seq, max_len,
+                                  scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+    del kp, vp, q, o, l
+    torch.cuda.empty_cache()
+
+
 def test_paged_bad_block_table_is_reported(attn):
     """A block-table entry outside the pool is reported, never read."""
     import torch
