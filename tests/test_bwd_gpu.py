@@ -121,3 +121,38 @@ def test_backward_gqa_full_size(attn):
                                                4001, heads=list(range(8)))
     check_both(got, got_given, ref, sc, "bf16", "GQA N=8192",
                sel=lambda x, i: x[0, :8] if i == 0 else x[0, :1])
+
+
+def test_dq_past_2_31_elements_sampled(attn):
+    """Q, dO, O and dQ of 2.29e9 elements (B=1, Hq=128, Hkv=8, N=140,000 with a ragged last
+    tile, d=128, bf16, causal), so that element offsets pass 2^31 in the last heads.  A query
+    row's gradient depends only on its own q, o, do, L and its visible keys, so each sampled row
+    of dQ is checked against the oracle run on that row alone: one query against its visible
+    keys, without a mask (the GPU backward runs on the GPU forward's O and L, and the check is
+    check_grad's with the scales for that source of O)."""
+    import torch
+
+    cfg = syn.PrefillConfig("bigbwd", 1, 128, 8, 140000, 140000, 128, "bf16", True, 6101)
+    assert cfg.B * cfg.Hq * cfg.N_q * cfg.d > 2 ** 31
+    q, k, v = cfg.device_inputs("cuda")
+    do = syn.device_normal(q.shape, cfg.seed + 7, cfg.dtype, "cuda")
+    o, lse = attn.attn_fwd(q, k, v, causal=True, scale=cfg.scale)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, do, lse, causal=True, scale=cfg.scale)
+    assert attn.attn_poll_status() == 0
+    del dk, dv
+    G = cfg.Hq // cfg.Hkv
+    rng = np.random.default_rng(6102)
+    bits = lambda t: syn.tensor_to_bits(t.contiguous())
+    for h in (0, 61, cfg.Hq - 1):
+        rows = sorted({0, 1, 127, 128, cfg.N_q - 1, *rng.integers(0, cfg.N_q, 3).tolist()})
+        for i in rows:
+            vis = i + 1  # N_q == N_kv: row i sees keys 0 .. i
+            qr, dor = bits(q[0, h, i:i + 1]), bits(do[0, h, i:i + 1])
+            kr, vr = bits(k[0, h // G, :vis]), bits(v[0, h // G, :vis])
+            rq, _, _, _, _, sc = attention_backward(qr, kr, vr, dor, cfg.dtype, 1, 1, 1, 1, vis,
+                                                    cfg.d, False, cfg.scale, error_scales=True)
+            got = dq[0, h, i].float().cpu().numpy().reshape(1, 1, 1, cfg.d)
+            check_grad("dq", got, rq, sc.row[0], sc.elem[0], cfg.dtype,
+                       f"2^31+ elements, head {h} row {i}")
+    del q, k, v, do, o, lse, dq
+    torch.cuda.empty_cache()
