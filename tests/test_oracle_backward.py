@@ -99,6 +99,29 @@ def test_grouped_heads_sum_their_contributions():
     np.testing.assert_allclose(sum(p[2] for p in parts), dv, rtol=0, atol=1e-12)
 
 
+def test_one_row_problem_gives_that_rows_query_gradient():
+    """dQ_i = scale * sum_j P_ij (dP_ij - D_i) K_j involves only row i's q, do, its O and L and
+    the keys it sees, so one query against its visible keys without a mask gives the same row of
+    dQ and the same rounding scales as the whole causal problem (the reduction the large-size
+    GPU test samples rows with)."""
+    B, Hq, Hkv, N, d, dt = 1, 4, 2, 300, 64, "bf16"
+    cfg = syn.PrefillConfig("row", B, Hq, Hkv, N, N, d, dt, True, 5)
+    q, k, v = cfg.host_inputs()
+    do = syn.host_normal_bits((B, Hq, N, d), 12, dt)
+    full = attention_backward(q, k, v, do, dt, B, Hq, Hkv, N, N, d, True, cfg.scale,
+                              error_scales=True)
+    G = Hq // Hkv
+    for h in range(Hq):
+        for i in (0, 1, 127, 128, 171, N - 1):
+            r = attention_backward(q[:, h:h + 1, i:i + 1], k[:, h // G:h // G + 1, :i + 1],
+                                   v[:, h // G:h // G + 1, :i + 1], do[:, h:h + 1, i:i + 1], dt,
+                                   1, 1, 1, 1, i + 1, d, False, cfg.scale, error_scales=True)
+            np.testing.assert_allclose(r[0][0, 0, 0], full[0][0, h, i], rtol=0, atol=1e-14)
+            np.testing.assert_allclose(r[5].row[0][0, 0, 0], full[5].row[0][0, h, i], rtol=1e-12)
+            np.testing.assert_allclose(r[5].elem[0][0, 0, 0], full[5].elem[0][0, h, i],
+                                       rtol=1e-12, atol=1e-300)
+
+
 def test_stored_output_changes_only_the_d_term():
     """D from O rounded to the storage type: dV is unchanged, and dQ, dK move only by the
     rounding of D (dS changes by -P * dD)."""
