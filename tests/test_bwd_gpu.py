@@ -102,6 +102,26 @@ def test_backward_small(attn, shape):
     check_both(got, got_given, ref, sc, dt, f"shape {shape}")
 
 
+@pytest.mark.parametrize("nq,nkv", [(0, 300), (300, 0)], ids=["no_queries", "no_keys"])
+def test_backward_with_an_empty_side_is_zero(attn, nq, nkv):
+    """No (query, key) pair: every gradient is exactly zero (outputs pre-filled with NaN)."""
+    import torch
+
+    dt = torch.bfloat16
+    q = torch.randn((2, 4, nq, 128), device="cuda").to(dt)
+    k = torch.randn((2, 2, nkv, 128), device="cuda").to(dt)
+    v = torch.randn_like(k)
+    o = torch.zeros_like(q)
+    do = torch.randn_like(q)
+    lse = torch.full((2, 4, nq), float("-inf"), device="cuda")
+    nan = lambda t: torch.full_like(t, float("nan"))
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, do, lse, causal=True, scale=0.125, dq=nan(q),
+                               dk=nan(k), dv=nan(v))
+    assert attn.attn_poll_status() == 0
+    for t in (dq, dk, dv):
+        assert torch.equal(t, torch.zeros_like(t))
+
+
 def test_backward_deterministic(attn):
     import torch
 
